@@ -1,0 +1,130 @@
+"""GEMM for one NVIDIA GB300 GPU: C = alpha * op(A) * op(B) + beta * C, row-major.
+
+Thin Python face of the C ABI in include/gemm_gb300.h.  The functions take torch CUDA
+tensors (or raw device addresses as ints), pass their addresses, sizes and the current
+CUDA stream to the library, and raise GemmError on a non-OK status.  All arithmetic runs
+in the library's CUDA kernels; torch only owns the memory and the stream.
+
+    gemm_sgemm_f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+    gemm_hgemm_f16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import GEMM_OP_N, GEMM_OP_T, STATUS, GemmError, library_path, load
+
+__all__ = [
+    "GEMM_OP_N", "GEMM_OP_T", "GemmError", "gemm_sgemm_f32", "gemm_hgemm_f16f32",
+    "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
+    "library_path", "load", "matmul",
+]
+
+
+def _op(op) -> int:
+    if op in (GEMM_OP_N, "N", "n"):
+        return GEMM_OP_N
+    if op in (GEMM_OP_T, "T", "t"):
+        return GEMM_OP_T
+    raise ValueError(f"op must be 'N' or 'T', got {op!r}")
+
+
+def _addr(x, want_dtype=None) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("operands must be torch tensors or device addresses")
+    if not x.is_cuda:
+        raise ValueError("operands must live in CUDA device memory")
+    if want_dtype is not None and x.dtype != want_dtype:
+        raise TypeError(f"expected {want_dtype}, got {x.dtype}")
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmError(status, what)
+
+
+def gemm_sgemm_f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    import torch
+
+    st = load().gemm_sgemm_f32(_op(opA), _op(opB), M, N, K, alpha, _addr(A, torch.float32), lda,
+                               _addr(B, torch.float32), ldb, beta, _addr(C, torch.float32), ldc,
+                               _stream(stream))
+    _check(st, "gemm_sgemm_f32")
+
+
+def gemm_hgemm_f16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    import torch
+
+    st = load().gemm_hgemm_f16f32(_op(opA), _op(opB), M, N, K, alpha, _addr(A, torch.float16),
+                                  lda, _addr(B, torch.float16), ldb, beta,
+                                  _addr(C, torch.float32), ldc, _stream(stream))
+    _check(st, "gemm_hgemm_f16f32")
+
+
+def gemm_get_device_status(stream=None) -> int:
+    """Status code of the device error word (waits for the stream, then clears it)."""
+    return int(load().gemm_get_device_status(_stream(stream)))
+
+
+def gemm_status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+def gemm_version() -> int:
+    return int(load().gemm_version())
+
+
+def gemm_tile_raster(t, tiles_m, tiles_n, log_group):
+    """(tile_m, tile_n) of tile t under the library's grouped raster (host function)."""
+    tm, tn = ctypes.c_int64(), ctypes.c_int64()
+    st = load().gemm_tile_raster(t, tiles_m, tiles_n, log_group, ctypes.byref(tm),
+                                 ctypes.byref(tn))
+    _check(st, "gemm_tile_raster")
+    return tm.value, tn.value
+
+
+def matmul(A, B, C=None, alpha=1.0, beta=0.0, opA="N", opB="N", stream=None):
+    """Tensor-level convenience over the two entry points.
+
+    A and B are 2-D CUDA tensors holding the STORED matrices (row stride = leading
+    dimension, unit column stride); fp32 operands go to gemm_sgemm_f32, fp16 operands to
+    gemm_hgemm_f16f32.  C (fp32, M x N) is created when omitted (then beta must be 0).
+    """
+    import torch
+
+    for x in (A, B):
+        if x.dim() != 2 or x.stride(1) != 1:
+            raise ValueError("operands must be 2-D with unit column stride")
+    M = A.shape[0] if _op(opA) == GEMM_OP_N else A.shape[1]
+    K = A.shape[1] if _op(opA) == GEMM_OP_N else A.shape[0]
+    N = B.shape[1] if _op(opB) == GEMM_OP_N else B.shape[0]
+    kb = B.shape[0] if _op(opB) == GEMM_OP_N else B.shape[1]
+    if kb != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {kb}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.shape != (M, N) or C.stride(1) != 1 or C.dtype != torch.float32:
+        raise ValueError("C must be fp32, M x N, unit column stride")
+    fn = gemm_sgemm_f32 if A.dtype == torch.float32 else gemm_hgemm_f16f32
+    fn(opA, opB, M, N, K, alpha, A, max(A.stride(0), 1), B, max(B.stride(0), 1), beta, C,
+       max(C.stride(0), 1), stream)
+    return C

@@ -1,0 +1,158 @@
+// Host side of the C ABI: argument validation, BLAS quick returns and dispatch to the
+// SGEMM (CUDA-core FFMA) and HGEMM (tcgen05) launchers.  No device memory is allocated.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gemm_internal.h"
+
+namespace gemm {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices];
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+}  // namespace
+
+bool current_device(DeviceInfo &info)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        d.smem_optin = size_t(optin);
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    info = g_dev[dev];
+    return true;
+}
+
+// Shared argument checks of both precisions (row-major rules of include/gemm_gb300.h).
+static gemm_status_t check_common(int opA, int opB, int64_t M, int64_t N, int64_t K,
+                                  const void *A, int64_t lda, const void *B, int64_t ldb,
+                                  const void *C, int64_t ldc, bool need_ab)
+{
+    if ((opA != GEMM_OP_N && opA != GEMM_OP_T) || (opB != GEMM_OP_N && opB != GEMM_OP_T))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    const int64_t min_lda = opA == GEMM_OP_N ? K : M;
+    const int64_t min_ldb = opB == GEMM_OP_N ? N : K;
+    if (lda < (min_lda > 1 ? min_lda : 1) || ldb < (min_ldb > 1 ? min_ldb : 1) ||
+        ldc < (N > 1 ? N : 1))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (need_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_VALUE;
+    return GEMM_OK;
+}
+
+static gemm_status_t from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+}  // namespace gemm
+
+using namespace gemm;
+
+extern "C" {
+
+gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float beta, float *C, int64_t ldc, void *stream)
+{
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
+    if (s != GEMM_OK || M == 0 || N == 0) return s;
+    if (!aligned(C, 4) || (need_ab && (!aligned(A, 4) || !aligned(B, 4))))
+        return GEMM_ERR_MISALIGNED;
+    DeviceInfo dev;
+    if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!need_ab) {
+        if (beta == 1.0f) return GEMM_OK;
+        return from_cuda(launch_scale(M, N, beta, C, ldc, st));
+    }
+    return from_cuda(launch_sgemm(dev, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st));
+}
+
+gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                const uint16_t *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, void *stream)
+{
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
+    if (s != GEMM_OK || M == 0 || N == 0) return s;
+    if (!aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    if (need_ab && (!aligned(A, 16) || !aligned(B, 16) || (lda % 8) != 0 || (ldb % 8) != 0))
+        return GEMM_ERR_MISALIGNED;
+    if (need_ab && (lda > (int64_t(1) << 35) || ldb > (int64_t(1) << 35)))
+        return GEMM_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!need_ab) {
+        if (beta == 1.0f) return GEMM_OK;
+        return from_cuda(launch_scale(M, N, beta, C, ldc, st));
+    }
+    return launch_hgemm(dev, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st);
+}
+
+gemm_status_t gemm_get_device_status(void *stream)
+{
+    DeviceInfo dev;
+    if (!current_device(dev)) return GEMM_ERR_NO_DEVICE;
+    return read_and_clear_device_status(static_cast<cudaStream_t>(stream));
+}
+
+const char *gemm_status_string(gemm_status_t status)
+{
+    switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: bad size, op, leading dimension or pointer";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: pointer or leading dimension breaks the alignment rule";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: size beyond the library limits";
+    case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: the CUDA runtime refused the launch";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded barrier wait";
+    case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable sm_103 device is current";
+    }
+    return "unknown gemm_status_t";
+}
+
+int gemm_version(void) { return 100; }
+
+gemm_status_t gemm_tile_raster(int64_t t, int64_t tiles_m, int64_t tiles_n, int log_group,
+                               int64_t *tile_m, int64_t *tile_n)
+{
+    if (tile_m == nullptr || tile_n == nullptr || tiles_m <= 0 || tiles_n <= 0 ||
+        log_group < 0 || log_group > 16 || t < 0 || t >= tiles_m * tiles_n)
+        return GEMM_ERR_INVALID_VALUE;
+    int64_t tm = 0, tn = 0;
+    raster(t, tiles_m, tiles_n, log_group, tm, tn);
+    *tile_m = tm;
+    *tile_n = tn;
+    return GEMM_OK;
+}
+
+}  // extern "C"

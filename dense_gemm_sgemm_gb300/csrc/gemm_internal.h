@@ -1,0 +1,55 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gemm_gb300.h"
+
+namespace gemm {
+
+// Grouped tile raster (copecc "GEMM" page, section "线程块网格重排"): consecutive tile
+// indices walk down a group of 2^log_group tile rows before moving to the next tile
+// column, so the tiles running at the same time share A rows and B columns in L2.
+__host__ __device__ __forceinline__ void raster(int64_t t, int64_t tiles_m, int64_t tiles_n,
+                                                int log_group, int64_t &tm, int64_t &tn)
+{
+    const int64_t group_rows = int64_t(1) << log_group;
+    const int64_t per_group = group_rows * tiles_n;
+    const int64_t g = t / per_group;
+    const int64_t first = g * group_rows;
+    int64_t rows = tiles_m - first;
+    if (rows > group_rows) rows = group_rows;
+    const int64_t r = t - g * per_group;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+};
+
+// Cached per-device properties of the current device; false if there is none.
+bool current_device(DeviceInfo &info);
+
+// Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
+cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
+                         int64_t K, float alpha, const float *A, int64_t lda, const float *B,
+                         int64_t ldb, float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+cudaError_t launch_scale(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
+                         cudaStream_t stream);
+
+// Returns GEMM_OK, GEMM_ERR_MISALIGNED or GEMM_ERR_LAUNCH.
+gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
+                           int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                           const uint16_t *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                           cudaStream_t stream);
+
+// Reads and clears the device error word (synchronises `stream`).
+gemm_status_t read_and_clear_device_status(cudaStream_t stream);
+
+}  // namespace gemm

@@ -1,0 +1,123 @@
+/*
+ * gemm_gb300.h -- C ABI of a GEMM library for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Every entry point computes the general matrix product of the copecc.github.io "GEMM"
+ * page (section "核心问题与运算特征"):
+ *
+ *     C = alpha * op(A) * op(B) + beta * C          op(A): M x K, op(B): K x N, C: M x N
+ *
+ * with each C[i][j] the dot product of row i of op(A) and column j of op(B) (the same
+ * section; also yekq.top "LeetGPU 第二题", section "题目描述").
+ *
+ * Layout.  All matrices are ROW-MAJOR.  A leading dimension is the element distance
+ * between the first elements of two consecutive stored rows, and may exceed the logical
+ * row length when rows are padded (copecc "GEMM" page, section "Leading Dimension (lda,
+ * ldb, ldc)").  The transpose flags choose how a buffer is read (the role the op
+ * arguments play in cublasSgemm on the ssxxe.cn page, section "三、cuBLAS 实现方式探究",
+ * restated for row-major storage):
+ *     opA = GEMM_OP_N: A stored M x K, op(A)[i][k] = A[i*lda + k], lda >= max(1, K)
+ *     opA = GEMM_OP_T: A stored K x M, op(A)[i][k] = A[k*lda + i], lda >= max(1, M)
+ *     opB = GEMM_OP_N: B stored K x N, op(B)[k][j] = B[k*ldb + j], ldb >= max(1, N)
+ *     opB = GEMM_OP_T: B stored N x K, op(B)[k][j] = B[j*ldb + k], ldb >= max(1, K)
+ *     C stored M x N, C[i][j] at C[i*ldc + j], ldc >= max(1, N)
+ *
+ * Ownership.  A, B and C are device memory owned by the caller; the library never frees,
+ * retains or allocates per call.  C must not overlap A or B.
+ *
+ * Asynchrony.  A call validates its arguments on the host, launches on `stream` (a
+ * cudaStream_t passed as void*; NULL means the legacy default stream of the current
+ * device) and returns without waiting.  The return value reports argument errors and
+ * launch errors only; gemm_get_device_status() reports errors raised inside a kernel.
+ * Nothing aborts or exits the process.
+ *
+ * BLAS conventions.  M == 0 or N == 0: nothing is launched and GEMM_OK is returned.
+ * K == 0 or alpha == 0: C = beta * C.  beta == 0: C is written without being read, so
+ * NaN or Inf already in C does not propagate.  alpha and beta are host values.
+ *
+ * Thread safety.  Calls may come from several host threads; calls that write the same C
+ * concurrently race, as with any BLAS.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+/* Symbols of this header are the only ones the shared library exports. */
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,  /* bad size, op, leading dimension or NULL pointer */
+    GEMM_ERR_MISALIGNED = 2,     /* pointer or leading dimension breaks the alignment rule */
+    GEMM_ERR_UNSUPPORTED = 3,    /* size beyond the library's limits (see each call) */
+    GEMM_ERR_LAUNCH = 4,         /* the CUDA runtime refused the launch */
+    GEMM_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on a barrier (bounded wait) */
+    GEMM_ERR_NO_DEVICE = 6       /* no usable sm_103 device is current */
+} gemm_status_t;
+
+/*
+ * Strict-FP32 GEMM (SGEMM) on the CUDA cores: every product and sum is an IEEE fp32
+ * fused multiply-add, never TF32 and never a reduced-precision tensor operation.
+ * A, B, C: 4-byte aligned fp32 device pointers; any leading dimension is accepted (the
+ * 16-byte vector paths are used only where pointer and leading dimension allow them).
+ * Limits: M, N, K < 2^31.
+ */
+GEMM_API gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * fp16-input GEMM with fp32 accumulation and fp32 output on the tcgen05 tensor cores
+ * (the mixed-precision mode of the copecc "GEMM" page, section "Batched 执行与混合精度", and
+ * of the dandandamowang.xyz "GEMM优化（二）" page): products of IEEE binary16 inputs are
+ * summed in fp32, then C = alpha * sum + beta * C in fp32.
+ * A, B: IEEE binary16 bit patterns (uint16_t), base 16-byte aligned, and lda, ldb
+ * multiples of 8 elements (the tensor-memory-access unit moves 16-byte granules);
+ * otherwise GEMM_ERR_MISALIGNED.  C: fp32, 4-byte aligned, any ldc.
+ * Limits: M, N, K < 2^31; lda, ldb < 2^36 bytes.
+ */
+GEMM_API gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                const uint16_t *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, void *stream);
+
+/*
+ * Waits for `stream`, then returns and clears the error word that kernels of this library
+ * set on the current device when a bounded barrier wait expires (GEMM_ERR_DEVICE_TIMEOUT),
+ * or GEMM_OK.  A kernel that sets the word leaves its output tile unwritten.
+ */
+GEMM_API gemm_status_t gemm_get_device_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+GEMM_API const char *gemm_status_string(gemm_status_t status);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+GEMM_API int gemm_version(void);
+
+/*
+ * Tile raster used by the kernels (a host function: needs no GPU).  It maps the t-th tile
+ * of a tiles_m x tiles_n grid of output tiles to (tile_m, tile_n) so that consecutive
+ * tiles sweep a group of 2^log_group tile rows column by column, which keeps the operand
+ * tiles they share resident in L2 (copecc "GEMM" page, section "线程块网格重排 (Thread Block
+ * Swizzling)"; with tiles_m = 2^log_group this is exactly that section's mapping).  The
+ * last group may be shorter.  Returns GEMM_ERR_INVALID_VALUE for t outside the grid,
+ * non-positive grid sizes, log_group outside [0, 16] or NULL outputs.
+ */
+GEMM_API gemm_status_t gemm_tile_raster(int64_t t, int64_t tiles_m, int64_t tiles_n, int log_group,
+                               int64_t *tile_m, int64_t *tile_n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

@@ -1,0 +1,99 @@
+"""Shared helpers of the parity tests: run the library, run the oracle, compare.
+
+Acceptance (per element, from the definition of the method and the stated tolerances):
+    |C - C_ref| <= tol * (|alpha| * sum_k |a_ik b_kj| + |beta| * |Cin_ij|) + ulp32(|C_ref|)
+with tol = 1e-5 for strict FP32 and 2e-3 for fp16 inputs with fp32 accumulation, and bit
+equality when every input is a small integer (all partial sums are then exact in fp32).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from dense_gemm_sgemm_gb300 import gemm_hgemm_f16f32, gemm_sgemm_f32, workloads
+
+TOL = {"f32": 1e-5, "f16": 2e-3}
+
+
+def to_device(inputs: dict) -> dict:
+    return {k: v.cuda() for k, v in inputs.items()}
+
+
+def run_library(w: workloads.Workload, dev: dict, stream=None):
+    fn = gemm_sgemm_f32 if w.dtype == "f32" else gemm_hgemm_f16f32
+    fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, dev["A"], w.lda, dev["B"], w.ldb, w.beta,
+       dev["C"], w.ldc, stream)
+
+
+def _np_in(t: torch.Tensor, dtype: str):
+    a = t.contiguous().cpu().numpy()
+    return a.view(np.uint16) if dtype == "f16" else a
+
+
+def oracle_full(w: workloads.Workload, inputs: dict):
+    """Oracle C (M x N) and absdot for the whole problem."""
+    return oracle.gemm(w.opA, w.opB, w.M, w.N, w.K, w.alpha, _np_in(inputs["A"], w.dtype),
+                       w.lda, _np_in(inputs["B"], w.dtype), w.ldb, w.beta,
+                       inputs["C"].numpy(), w.ldc, dtype=w.dtype, want_absdot=True)
+
+
+def oracle_points(w: workloads.Workload, inputs: dict, rows, cols):
+    return oracle.gemm_points(w.opA, w.opB, w.M, w.N, w.K, w.alpha,
+                              _np_in(inputs["A"], w.dtype), w.lda,
+                              _np_in(inputs["B"], w.dtype), w.ldb, w.beta,
+                              inputs["C"].numpy(), w.ldc, rows, cols, dtype=w.dtype)
+
+
+def assert_close(w, got, ref, absdot, cin, integer=False, where=""):
+    got = np.asarray(got, dtype=np.float32)
+    ref = np.asarray(ref, dtype=np.float32)
+    assert got.shape == ref.shape
+    if integer:
+        bad = got.view(np.uint32) != ref.view(np.uint32)
+        if bad.any():
+            i = np.argwhere(bad)[0]
+            raise AssertionError(f"{w.name}{where}: not bit-exact at {tuple(i)}: "
+                                 f"{got[tuple(i)]} vs {ref[tuple(i)]} ({bad.sum()} elements)")
+        return
+    bound = oracle.tolerance_bound(ref, absdot, w.alpha, w.beta, cin, TOL[w.dtype])
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bad = ~(err <= bound)  # NaN in got counts as bad
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{w.name}{where}: {bad.sum()} elements out of bound; first at "
+                             f"{i}: got {got[i]} ref {ref[i]} err {err[i]:.3e} bound {bound[i]:.3e}")
+
+
+def check_full(w, inputs, dev_c, integer=False):
+    ref, absdot = oracle_full(w, inputs)
+    got = dev_c.cpu().numpy()[:, : w.N]
+    cin = inputs["C"].numpy()[:, : w.N] if w.beta != 0.0 else None
+    assert_close(w, got, ref, absdot, cin, integer)
+
+
+def sample_points(w, n_random=4096, seed=0, tile=(128, 128)):
+    """Random positions plus every tile-edge row and column (first/last of each tile)."""
+    rng = np.random.default_rng(seed)
+    rows = list(rng.integers(0, w.M, n_random))
+    cols = list(rng.integers(0, w.N, n_random))
+    bm, bn = tile
+    edge_r = sorted({x for t in range(0, w.M, bm) for x in (t, min(t + bm, w.M) - 1)} | {w.M - 1})
+    edge_c = sorted({x for t in range(0, w.N, bn) for x in (t, min(t + bn, w.N) - 1)} | {w.N - 1})
+    for r in edge_r:
+        rows += [r] * 8
+        cols += list(rng.integers(0, w.N, 8))
+    for c in edge_c:
+        cols += [c] * 8
+        rows += list(rng.integers(0, w.M, 8))
+    return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
+
+
+def check_sampled(w, inputs, dev_c, n_random=4096, seed=0):
+    rows, cols = sample_points(w, n_random, seed)
+    ref, absdot = oracle_points(w, inputs, rows, cols)
+    r_t = torch.as_tensor(rows, device=dev_c.device)
+    c_t = torch.as_tensor(cols, device=dev_c.device)
+    got = dev_c[r_t, c_t].cpu().numpy()
+    cin = inputs["C"].numpy()[rows, cols] if w.beta != 0.0 else None
+    assert_close(w, got, ref, absdot, cin, where=" (sampled)")

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every symbol
+the header declares, validates arguments before touching a device, and its tile raster
+reproduces the worked example of the pages."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_sgemm_gb300 as g
+from dense_gemm_sgemm_gb300 import _lib, build
+from tests import golden_io
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gemm_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "gemm_sgemm_f32" in names and "gemm_hgemm_f16f32" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in _lib.STATUS.items():
+        assert g.gemm_status_string(code).startswith(name)
+    assert "unknown" in g.gemm_status_string(99)
+    assert g.gemm_version() >= 100
+
+
+def test_tile_raster_matches_block_swizzle_example(lib):
+    d = golden_io.read("block_swizzle_16.txt")
+    log_tile = golden_io.scalar(d, "log_tile")
+    count = golden_io.scalar(d, "count")
+    side = 1 << log_tile
+    assert count == side * side
+    picture = [[int(x) for x in row] for row in d["row"]]
+    for t in range(count):
+        tm, tn = g.gemm_tile_raster(t, side, side, log_tile)
+        assert picture[tm][tn] == t
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,log_group", [(7, 5, 1), (13, 9, 3), (1, 40, 2), (33, 1, 4)])
+def test_tile_raster_is_a_bijection_with_grouped_order(lib, tiles_m, tiles_n, log_group):
+    seen = set()
+    prev = None
+    for t in range(tiles_m * tiles_n):
+        tm, tn = g.gemm_tile_raster(t, tiles_m, tiles_n, log_group)
+        assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
+        seen.add((tm, tn))
+        if prev is not None and tm // (1 << log_group) == prev[0] // (1 << log_group):
+            assert tn >= prev[1]  # within a group, columns never go back
+        prev = (tm, tn)
+    assert len(seen) == tiles_m * tiles_n
+    with pytest.raises(g.GemmError):
+        g.gemm_tile_raster(tiles_m * tiles_n, tiles_m, tiles_n, log_group)
+
+
+def test_argument_validation_needs_no_device(lib):
+    f = lib.gemm_sgemm_f32
+    h = lib.gemm_hgemm_f16f32
+    P = 4096  # a fake, never dereferenced address: every call below returns before any launch
+    assert f(2, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 1      # bad op
+    assert f(0, 0, -1, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 1     # negative M
+    assert f(0, 0, 4, 4, 4, 1.0, P, 3, P, 4, 0.0, P, 4, None) == 1      # lda < K
+    assert f(1, 0, 4, 4, 4, 1.0, P, 3, P, 4, 0.0, P, 4, None) == 1      # lda < M (op T)
+    assert f(0, 1, 4, 4, 5, 1.0, P, 5, P, 4, 0.0, P, 4, None) == 1      # ldb < K (op T)
+    assert f(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 3, None) == 1      # ldc < N
+    assert f(0, 0, 4, 4, 4, 1.0, None, 4, P, 4, 0.0, P, 4, None) == 1   # NULL A
+    assert f(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, None, 4, None) == 1   # NULL C
+    assert f(0, 0, 0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, None) == 0  # empty: no launch
+    assert f(0, 0, 1 << 31, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 3
+    assert f(0, 0, 4, 4, 4, 1.0, P + 2, 4, P, 4, 0.0, P, 4, None) == 2  # A not 4-byte aligned
+    assert h(0, 0, 4, 4, 8, 1.0, P + 8, 8, P, 8, 0.0, P, 4, None) == 2  # A not 16-byte aligned
+    assert h(0, 0, 4, 8, 4, 1.0, P, 4, P, 8, 0.0, P, 8, None) == 2      # lda not a multiple of 8
+    assert h(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 2
+    # K == 0 or alpha == 0 does not need A or B
+    assert f(0, 0, 0, 0, 0, 0.0, None, 1, None, 1, 0.0, None, 1, None) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    x = torch.zeros(4, 4)
+    with pytest.raises(ValueError):
+        g.gemm_sgemm_f32("N", "N", 4, 4, 4, 1.0, x, 4, x, 4, 0.0, x, 4, stream=0)

@@ -1,0 +1,161 @@
+"""Parity of the strict-FP32 path (gemm_sgemm_f32) against the CPU oracle."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_sgemm_gb300 import GemmError, gemm_get_device_status, gemm_sgemm_f32, workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, inputs=None):
+    inputs = inputs if inputs is not None else workloads.make_inputs(w)
+    dev = parity.to_device(inputs)
+    parity.run_library(w, dev)
+    torch.cuda.synchronize()
+    assert gemm_get_device_status() == 0
+    return inputs, dev
+
+
+def test_256_cube_uniform():
+    w = workloads.sgemm_256()
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"])
+
+
+def test_256_cube_integer_bit_exact():
+    w = workloads.sgemm_256(integer=True)
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"], integer=True)
+
+
+def test_ragged_1001x777x513_alpha_beta():
+    w = workloads.sgemm_ragged()
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"])
+
+
+@pytest.mark.parametrize("mn", [128, 256, 512, 1024, 2048])
+def test_sweep_full_oracle(mn):
+    w = workloads.sgemm_sweep(mn)
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"])
+
+
+@pytest.mark.parametrize("mn", [4096, 8192, 16384])
+def test_sweep_sampled(mn):
+    w = workloads.sgemm_sweep(mn)
+    inputs, dev = _run(w)
+    parity.check_sampled(w, inputs, dev["C"], n_random=2048)
+    assert torch.isfinite(dev["C"]).all()
+
+
+def test_4096_cube_sampled():
+    w = workloads.sgemm_cube(4096)
+    inputs, dev = _run(w)
+    parity.check_sampled(w, inputs, dev["C"], n_random=1024)
+
+
+_EDGE = [1, 2, 3, 5, 7, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+
+
+def _fuzz_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M, N, K = (int(rng.choice(_EDGE)) for _ in range(3))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
+def test_fuzz_shapes_ops_padding(opA, opB):
+    for i, (M, N, K) in enumerate(_fuzz_cases(24, seed=hash((opA, opB)) % 1000)):
+        pad = (i % 3, (i // 3) % 3, i % 2)  # unaligned lds exercise the 4-byte loaders
+        beta = 0.0 if i % 2 == 0 else -0.75
+        w = workloads.Workload(f"fuzz_{M}x{N}x{K}_{opA}{opB}", "f32", M, N, K, opA, opB,
+                               alpha=1.25, beta=beta, seed=100 + i, pad=pad)
+        inputs, dev = _run(w)
+        parity.check_full(w, inputs, dev["C"][:, : w.N].contiguous() if pad[2] else dev["C"])
+        if pad[2]:  # padding columns of C are never written
+            assert torch.isnan(dev["C"][:, w.N:]).all()
+
+
+@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
+def test_integer_bit_exact_all_ops(opA, opB):
+    w = workloads.Workload(f"int_{opA}{opB}", "f32", 300, 200, 1024, opA, opB, seed=7,
+                           dist_a="int4", dist_b="int4")
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"], integer=True)
+
+
+def test_misaligned_pointers_take_scalar_paths():
+    # Views that start one element into their buffers are 4-byte but not 16-byte aligned.
+    M, N, K = 150, 130, 70
+    g = torch.Generator().manual_seed(21)
+    Abuf = torch.rand(M * K + 1, generator=g) * 2 - 1
+    Bbuf = torch.rand(K * N + 1, generator=g) * 2 - 1
+    Cbuf = torch.rand(M * N + 1, generator=g) * 2 - 1
+    for opA, opB in itertools.product("NT", "NT"):
+        w = workloads.Workload(f"misaligned_{opA}{opB}", "f32", M, N, K, opA, opB, alpha=0.5,
+                               beta=2.0)
+        inputs = {"A": Abuf[1:].reshape(w.a_shape).clone(), "B": Bbuf[1:].reshape(w.b_shape).clone(),
+                  "C": Cbuf[1:].reshape(M, N).clone()}
+        dA, dB, dC = Abuf.cuda(), Bbuf.cuda(), Cbuf.cuda()
+        gemm_sgemm_f32(opA, opB, M, N, K, 0.5, dA[1:], w.lda, dB[1:], w.ldb, 2.0, dC[1:], N)
+        torch.cuda.synchronize()
+        parity.check_full(w, inputs, dC[1:].reshape(M, N))
+
+
+def test_beta_zero_ignores_nan_and_k_zero_alpha_zero():
+    M, N, K = 70, 90, 40
+    A = torch.randn(M, K, device="cuda")
+    B = torch.randn(K, N, device="cuda")
+    C = torch.full((M, N), float("nan"), device="cuda")
+    gemm_sgemm_f32("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)
+    torch.cuda.synchronize()
+    assert torch.isfinite(C).all()
+    Cin = torch.randn(M, N, device="cuda")
+    C = Cin.clone()
+    gemm_sgemm_f32("N", "N", M, N, 0, 1.0, None, K, None, N, 0.5, C, N)  # K == 0
+    torch.cuda.synchronize()
+    assert torch.equal(C, Cin * 0.5)
+    C = Cin.clone()
+    gemm_sgemm_f32("N", "N", M, N, K, 0.0, A, K, B, N, 0.0, C, N)  # alpha == 0, beta == 0
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.zeros_like(C))
+    C = Cin.clone()
+    gemm_sgemm_f32("N", "N", M, N, K, 0.0, A, K, B, N, 1.0, C, N)  # nothing to do
+    torch.cuda.synchronize()
+    assert torch.equal(C, Cin)
+    gemm_sgemm_f32("N", "N", 0, N, K, 1.0, A, K, B, N, 0.0, C, N)  # empty M
+    gemm_sgemm_f32("N", "N", M, 0, K, 1.0, A, K, B, N, 0.0, C, 1)  # empty N
+
+
+def test_invalid_arguments_raise_before_launch():
+    A = torch.zeros(4, 4, device="cuda")
+    with pytest.raises(GemmError) as e:
+        gemm_sgemm_f32("N", "N", 4, 4, 4, 1.0, A, 3, A, 4, 0.0, A, 4)  # lda < K
+    assert e.value.status == 1
+    with pytest.raises(GemmError) as e:
+        gemm_sgemm_f32("N", "N", 4, 4, 4, 1.0, 0, 4, A, 4, 0.0, A, 4)  # NULL A
+    assert e.value.status == 1
+    base = A.data_ptr() + 2  # not 4-byte aligned
+    with pytest.raises(GemmError) as e:
+        gemm_sgemm_f32("N", "N", 2, 2, 2, 1.0, base, 4, A, 4, 0.0, A, 4)
+    assert e.value.status == 2
+
+
+def test_streams_are_respected():
+    w = workloads.sgemm_ragged()
+    inputs = workloads.make_inputs(w)
+    dev = parity.to_device(inputs)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        parity.run_library(w, dev)
+    s.synchronize()
+    parity.check_full(w, inputs, dev["C"])
