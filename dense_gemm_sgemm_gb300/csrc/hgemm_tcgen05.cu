@@ -1,5 +1,38 @@
 // fp16-input / fp32-accumulate GEMM on the tcgen05 tensor cores of sm_103a.
+//
+// C = alpha * op(A) * op(B) + beta * C with A, B in IEEE binary16 and C in fp32
+// (copecc.github.io "GEMM" page, sections "核心问题与运算特征" and "Batched 执行与混合精度";
+// dandandamowang.xyz "GEMM优化（二）": fp16 inputs, fp32 accumulator).  The pages reach the
+// tensor cores through WMMA fragments on one warp at a time; on Blackwell the same
+// contraction is issued by ONE thread per CTA as tcgen05.mma, with operands read straight
+// from shared memory through matrix descriptors and the fp32 accumulator kept in tensor
+// memory (TMEM).  The kernel is persistent and warp-specialised:
+//
+//   warp 0      TMA producer: one elected lane streams BK-wide K slices of the A and B
+//               tiles into a STAGES-deep shared-memory ring (cp.async.bulk.tensor with
+//               128-byte swizzle; the pages' cp.async double buffer of the "v4" section,
+//               moved to the tensor-memory-access unit and deepened);
+//   warp 1      MMA issuer and TMEM owner: allocates 512 TMEM columns (two 128 x 256 fp32
+//               accumulators), issues 4 tcgen05.mma (M=128, N=256, K=16) per slice and
+//               returns each slice to the producer with tcgen05.commit;
+//   warps 2-5   epilogue: tcgen05.ld the finished accumulator (one TMEM lane = one row of
+//               the tile), apply C = alpha * acc + beta * C and store with 128-bit stores,
+//               while warp 1 already accumulates the next tile into the other buffer.
+//
+// Tiles are visited in the grouped raster of the copecc "线程块网格重排" section.  Ragged M,
+// N and K need no special code: TMA fills out-of-range elements with zeros, which add
+// nothing to the dot products, and the epilogue predicates its stores.
+//
+// Every wait on an mbarrier is bounded: when a wait expires the kernel records
+// GEMM_ERR_DEVICE_TIMEOUT in g_device_status, stops all roles, waits (bounded) for its own
+// copies and MMAs in flight, frees its TMEM and returns.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
 
 #include "gemm_internal.h"
 
@@ -8,11 +41,489 @@ namespace gemm {
 // Error word raised by kernels whose bounded barrier waits expire (0 = no error).
 __device__ unsigned int g_device_status = 0;
 
-gemm_status_t launch_hgemm(const DeviceInfo &, int, int, int64_t, int64_t, int64_t, float,
-                           const uint16_t *, int64_t, const uint16_t *, int64_t, float, float *,
-                           int64_t, cudaStream_t)
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16, STAGES = 4;
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kAccCols = BN;        // fp32 columns per accumulator
+constexpr int kTmemCols = 2 * BN;   // two accumulators
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int kBarBytes = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kBarBytes + 1024;  // + alignment slack
+constexpr int kLogGroup = 3;
+
+struct HgemmParams {
+    int64_t M, N, K;
+    float *C;
+    int64_t ldc;
+    float alpha, beta;
+    int64_t tiles_m, tiles_n, num_tiles;
+    int num_kb;
+    int c_vec;               // C base 16-byte aligned and ldc % 4 == 0
+    uint64_t timeout_ns;     // limit of every barrier wait
+    int inject_stall;        // test hook: the producer never fills the first slice
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
-    return GEMM_ERR_UNSUPPORTED;
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of parity `parity` to complete.  Gives up (returns false) when the
+// CTA-wide abort flag is raised or after timeout_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag,
+                                          uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void raise_abort(volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(&g_device_status, 1u);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], one CTA, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld_32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a tcgen05 operand tile stored with the 128-byte
+// swizzle (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
+//   bits  0-13 start address >> 4       bits 16-29 leading byte offset >> 4
+//   bits 32-45 stride byte offset >> 4  bits 46-47 descriptor version (1)
+//   bits 49-51 base offset (0: tiles are 1024-byte aligned)
+//   bits 61-63 layout (2 = 128-byte swizzle)
+// K-major tiles (rows along M or N, 64 fp16 of K per 128-byte row): the stride byte
+// offset is the distance between 8-row groups (1024 bytes); the leading offset is unused.
+// MN-major tiles (rows along K, 64 fp16 of M or N per row): the leading byte offset is the
+// distance between 64-element column blocks, the stride byte offset between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t((addr >> 4) & 0x3FFFu)) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-9 and
+// 10-12 = 0), A/B major-ness in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn)
+{
+    return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+           (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int A_MN, int B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const HgemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+
+    const uint32_t sA = base;                          // STAGES x 16 KB
+    const uint32_t sB = base + STAGES * A_STAGE_BYTES; // STAGES x 32 KB
+    uint8_t *bar_area = smem + STAGES * STAGE_BYTES;
+    const uint32_t bar0 = smem_u32(bar_area);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * STAGES + 5));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * STAGES + 5) + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4 * 32);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(const_cast<uint32_t *>(tmem_slot))),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;  // per stage: a fill was issued / its parity
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int64_t tm, tn;
+                raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
+                const int32_t m0 = static_cast<int32_t>(tm * BM), n0 = static_cast<int32_t>(tn * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_expect_tx(fb, STAGE_BYTES);
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    const bool stall = p.inject_stall && t == blockIdx.x && kb == 0;
+                    if (!stall) {
+                        const int32_t k0 = kb * BK;
+                        const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
+                        const uint32_t b_dst = sB + stage * B_STAGE_BYTES;
+                        if (A_MN) {  // A stored K x M: two 64 (m) x 64 (k) boxes
+                            tma_load_2d(a_dst, &map_a, fb, m0, k0);
+                            tma_load_2d(a_dst + 8192, &map_a, fb, m0 + 64, k0);
+                        } else {     // A stored M x K: one 64 (k) x 128 (m) box
+                            tma_load_2d(a_dst, &map_a, fb, k0, m0);
+                        }
+                        if (B_MN) {  // B stored K x N: four 64 (n) x 64 (k) boxes
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0);
+                        } else {     // B stored N x K: one 64 (k) x 256 (n) box
+                            tma_load_2d(b_dst, &map_b, fb, k0, n0);
+                        }
+                    } else {
+                        filled &= ~(1u << stage);  // nothing in flight on this slot
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before the CTA's shared memory goes away.
+                for (int s = 0; s < STAGES; ++s)
+                    if ((filled >> s) & 1u) {
+                        const volatile int no_abort = 0;
+                        mbar_wait(full_bar(s), (fill_parity >> s) & 1u, &no_abort, 100000000ull);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true, issued = false;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, tmo)) {
+                    raise_abort(abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, tmo)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_tile = sA + stage * A_STAGE_BYTES;
+                    const uint32_t b_tile = sB + stage * B_STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // K-major: step 32 bytes along the swizzled 128-byte row.
+                        // MN-major: step 16 rows of 128 bytes.
+                        const uint64_t ad = A_MN ? smem_desc(a_tile + k * 2048, 8192, 1024)
+                                                 : smem_desc(a_tile + k * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc(b_tile + k * 2048, 8192, 1024)
+                                                 : smem_desc(b_tile + k * 32, 16, 1024);
+                        umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(accf_bar(acc));  // accumulator complete
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (!ok && issued) {
+                // Wait for the MMAs in flight before TMEM is released.
+                umma_commit(drain_bar);
+                const volatile int no_abort = 0;
+                mbar_wait(drain_bar, 0, &no_abort, 100000000ull);
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5; TMEM lane quarter = warp % 4)
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const float alpha = p.alpha, beta = p.beta;
+        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int64_t tm, tn;
+            raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
+            if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo)) {
+                raise_abort(abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const int64_t gm = tm * BM + row;
+            const bool row_ok = gm < p.M;
+            float *crow = p.C + (row_ok ? gm * p.ldc : 0);
+            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the predicated stores
+                tmem_ld_32(taddr + c * 32, v);
+                const int64_t gn0 = tn * BN + c * 32;
+                if (!row_ok || gn0 >= p.N) continue;
+                if (p.c_vec && gn0 + 32 <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4 o;
+                        float4 *dst = reinterpret_cast<float4 *>(crow + gn0 + 4 * j);
+                        if (beta != 0.0f) {
+                            const float4 ci = *dst;
+                            o.x = fmaf(alpha, v[4 * j + 0], beta * ci.x);
+                            o.y = fmaf(alpha, v[4 * j + 1], beta * ci.y);
+                            o.z = fmaf(alpha, v[4 * j + 2], beta * ci.z);
+                            o.w = fmaf(alpha, v[4 * j + 3], beta * ci.w);
+                        } else {
+                            o = make_float4(alpha * v[4 * j], alpha * v[4 * j + 1], alpha * v[4 * j + 2],
+                                            alpha * v[4 * j + 3]);
+                        }
+                        *dst = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t gn = gn0 + j;
+                        if (gn < p.N) {
+                            float *dst = crow + gn;
+                            *dst = beta != 0.0f ? fmaf(alpha, v[j], beta * *dst) : alpha * v[j];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acce_bar(acc));  // accumulator may be overwritten
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D fp16 tensor map over a row-major matrix of `rows` x `cols` (cols contiguous) with
+// leading dimension ld, read in boxes of box_cols x box_rows with the 128-byte swizzle.
+bool make_map(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t cols, int64_t ld,
+              uint32_t box_cols, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int A_MN, int B_MN>
+cudaError_t launch_t(int dev_id, int grid, const CUtensorMap &ma, const CUtensorMap &mb, const HgemmParams &p,
+                     cudaStream_t stream)
+{
+    auto kern = hgemm_tcgen05_kernel<A_MN, B_MN>;
+    static std::atomic<uint64_t> attr_set{0};
+    const uint64_t bit = uint64_t(1) << (dev_id & 63);
+    if (!(attr_set.load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit, std::memory_order_release);
+    }
+    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N, int64_t K,
+                           float alpha, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                           float beta, float *C, int64_t ldc, cudaStream_t stream)
+{
+    if (dev.smem_optin < size_t(SMEM_BYTES)) return GEMM_ERR_NO_DEVICE;
+    const int a_mn = opA == GEMM_OP_T;  // A stored K x M
+    const int b_mn = opB == GEMM_OP_N;  // B stored K x N
+    CUtensorMap ma, mb;
+    const bool ok_a = a_mn ? make_map(&ma, A, K, M, lda, 64, BK) : make_map(&ma, A, M, K, lda, BK, BM);
+    const bool ok_b = b_mn ? make_map(&mb, B, K, N, ldb, 64, BK) : make_map(&mb, B, N, K, ldb, BK, BN);
+    if (!ok_a || !ok_b) return GEMM_ERR_MISALIGNED;
+
+    HgemmParams p{};
+    p.M = M; p.N = N; p.K = K;
+    p.C = C; p.ldc = ldc;
+    p.alpha = alpha; p.beta = beta;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.num_kb = static_cast<int>((K + BK - 1) / BK);
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+    p.timeout_ns = 2000000000ull;
+    p.inject_stall = 0;
+    if (const char *e = std::getenv("GEMM_GB300_TEST_INJECT_STALL"); e && e[0] == '1') {
+        p.inject_stall = 1;
+        p.timeout_ns = 20000000ull;
+    }
+    const int grid = static_cast<int>(p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms);
+
+    cudaError_t e;
+    if (a_mn) e = b_mn ? launch_t<1, 1>(dev.device, grid, ma, mb, p, stream) : launch_t<1, 0>(dev.device, grid, ma, mb, p, stream);
+    else e = b_mn ? launch_t<0, 1>(dev.device, grid, ma, mb, p, stream) : launch_t<0, 0>(dev.device, grid, ma, mb, p, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
 gemm_status_t read_and_clear_device_status(cudaStream_t stream)

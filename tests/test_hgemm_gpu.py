@@ -1,0 +1,116 @@
+"""Parity of the fp16-input / fp32-accumulate tcgen05 path (gemm_hgemm_f16f32)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_sgemm_gb300 import GemmError, gemm_get_device_status, gemm_hgemm_f16f32, workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, inputs=None):
+    inputs = inputs if inputs is not None else workloads.make_inputs(w)
+    dev = parity.to_device(inputs)
+    parity.run_library(w, dev)
+    torch.cuda.synchronize()
+    assert gemm_get_device_status() == 0
+    return inputs, dev
+
+
+def _pad8(cols, extra=0):
+    return (-cols) % 8 + 8 * extra
+
+
+def test_small_full_oracle_all_ops():
+    for opA, opB in itertools.product("NT", "NT"):
+        M, N, K = 200, 300, 136
+        w0 = workloads.Workload("probe", "f16", M, N, K, opA, opB)
+        pad = (_pad8(w0.a_shape[1]), _pad8(w0.b_shape[1]), 0)
+        w = workloads.Workload(f"hgemm_small_{opA}{opB}", "f16", M, N, K, opA, opB, alpha=1.0,
+                               beta=0.0, seed=11, pad=pad)
+        inputs, dev = _run(w)
+        parity.check_full(w, inputs, dev["C"])
+
+
+@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
+def test_integer_bit_exact(opA, opB):
+    M, N, K = 384, 640, 1024
+    w = workloads.Workload(f"hgemm_int_{opA}{opB}", "f16", M, N, K, opA, opB, seed=5,
+                           dist_a="int4", dist_b="int4")
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"], integer=True)
+
+
+def test_persistent_tiles_and_double_buffered_accumulator():
+    # 18 x 10 = 180 tiles of 128 x 256: several CTAs run two tiles through both TMEM buffers
+    w = workloads.Workload("hgemm_2304x2560x192", "f16", 2304, 2560, 192, alpha=0.75, beta=0.5,
+                           seed=8)
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"])
+
+
+_EDGE = [1, 7, 8, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383]
+
+
+@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
+def test_fuzz_ragged_shapes(opA, opB):
+    rng = np.random.default_rng(10 * "NT".index(opA) + "NT".index(opB) + 77)
+    for i in range(12):
+        M, N, K = (int(rng.choice(_EDGE)) for _ in range(3))
+        w0 = workloads.Workload("probe", "f16", M, N, K, opA, opB)
+        pad = (_pad8(w0.a_shape[1], i % 2), _pad8(w0.b_shape[1], (i // 2) % 2), i % 3)
+        beta = 0.0 if i % 2 == 0 else 1.5
+        w = workloads.Workload(f"hgemm_fuzz_{M}x{N}x{K}_{opA}{opB}", "f16", M, N, K, opA, opB,
+                               alpha=-0.5, beta=beta, seed=200 + i, pad=pad)
+        inputs, dev = _run(w)
+        C = dev["C"]
+        parity.check_full(w, inputs, C[:, : w.N].contiguous() if pad[2] else C)
+        if pad[2]:
+            assert torch.isnan(C[:, w.N:]).all()
+
+
+@pytest.mark.parametrize("n", [2048, 4096, 8192])
+def test_square_sampled(n):
+    w = workloads.hgemm_square(n)
+    inputs, dev = _run(w)
+    parity.check_sampled(w, inputs, dev["C"], n_random=2048)
+    assert torch.isfinite(dev["C"]).all()
+
+
+def test_square_integer_2048_sampled_bit_exact():
+    w = workloads.hgemm_square(2048, integer=True, K=1024)
+    inputs, dev = _run(w)
+    rows, cols = parity.sample_points(w, 4096)
+    ref, _ = parity.oracle_points(w, inputs, rows, cols)
+    got = dev["C"][torch.as_tensor(rows).cuda(), torch.as_tensor(cols).cuda()].cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_linear_layer_opBT_beta1_sampled():
+    w = workloads.linear_fp16()
+    inputs, dev = _run(w)
+    parity.check_sampled(w, inputs, dev["C"], n_random=2048)
+
+
+def test_misaligned_operands_are_refused():
+    A = torch.zeros(64, 72, dtype=torch.float16, device="cuda")
+    C = torch.zeros(64, 64, device="cuda")
+    with pytest.raises(GemmError) as e:
+        gemm_hgemm_f16f32("N", "N", 64, 64, 64, 1.0, A, 68, A, 72, 0.0, C, 64)  # lda % 8
+    assert e.value.status == 2
+    with pytest.raises(GemmError) as e:
+        gemm_hgemm_f16f32("N", "N", 8, 8, 8, 1.0, A.data_ptr() + 2, 72, A, 72, 0.0, C, 64)
+    assert e.value.status == 2
+
+
+def test_beta_zero_ignores_nan():
+    M, N, K = 300, 504, 200  # lda = 200 and ldb = 504 are multiples of 8
+    A = torch.randn(M, K, device="cuda").half()
+    B = torch.randn(K, N, device="cuda").half()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    gemm_hgemm_f16f32("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)
+    torch.cuda.synchronize()
+    assert torch.isfinite(C).all()

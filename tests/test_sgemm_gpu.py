@@ -73,7 +73,7 @@ def _fuzz_cases(n, seed):
 
 @pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
 def test_fuzz_shapes_ops_padding(opA, opB):
-    for i, (M, N, K) in enumerate(_fuzz_cases(24, seed=hash((opA, opB)) % 1000)):
+    for i, (M, N, K) in enumerate(_fuzz_cases(24, seed=10 * "NT".index(opA) + "NT".index(opB))):
         pad = (i % 3, (i // 3) % 3, i % 2)  # unaligned lds exercise the 4-byte loaders
         beta = 0.0 if i % 2 == 0 else -0.75
         w = workloads.Workload(f"fuzz_{M}x{N}x{K}_{opA}{opB}", "f32", M, N, K, opA, opB,
