@@ -1,0 +1,437 @@
+"""Benchmark of the GEMM library on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-suite]
+
+A step is one call of the library on the headline workload: the strict-FP32 ragged
+problem M=1001, N=777, K=513, alpha=1.5, beta=-0.5 (uniform[-1,1] inputs from seed 1), the
+1001 x 513 x 777 case of the yekq.top "LeetGPU 第二题" page that exercises every tail of
+the tile grid.  Inputs are resident in HBM when the timed region starts; the 9.9 MB
+working set fits in L2, so L2 is flushed (a 512 MB write) before every timed step and
+only the GEMM itself sits between each step's CUDA events.
+
+Printed: ONE JSON line (rank 0) with the throughput (2*M*N*K / device time, TFLOP/s), the
+roofline of the kernel, the CPU oracle timed on the host cores, the end-to-end number
+through the public API with host buffers, the SM clocks seen during the timed region and,
+under "suite", the other headline shapes (fp32 4096^3 and 16384^2 x 1024, fp16 4096^3,
+8192^3 and the linear-layer 16384 x 4096 x 4096 problem) timed the same way.
+
+--impl reference times the CPU oracle (the only reference implementation of this path)
+on the same workload, on rank 0 only, as bounded row-slab samples.
+
+Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas of the
+same step (weak scaling); value = all replicas' flops / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/device time) FP32 & fp16→fp32, % of GB300 roofline"
+UNIT = "TFLOPS"
+# The pages' own best hand-written kernel on this exact workload (yekq.top "LeetGPU 第二题",
+# results table, v4 2-D register coarsening on an RTX 4090): 13848.77 GFLOPS.  Context only.
+PAGES_RAGGED_GFLOPS = 13848.77
+# FP32 FFMA roofline: 152 SMs x 128 FP32 lanes x 2 flop (fused multiply-add) x 2.07 GHz.
+SMS, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.070
+FFMA_PEAK_TFLOPS = SMS * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks during the run
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first sample arrive before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ helpers
+def whole_job_value(local_total_ms, steps, flops_per_step, world, device=None):
+    """Whole-job TFLOP/s of `world` replicas: every rank did `steps` steps of
+    `flops_per_step`; the job took as long as its slowest rank (max over ranks)."""
+    total_ms = float(local_total_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12, total_ms
+
+
+def _traffic_from_profile(kernel_file: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches today's source."""
+    path = os.path.join(ROOT, "profiles", profile)
+    src = os.path.join(ROOT, "dense_gemm_sgemm_gb300", "csrc", kernel_file)
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("source_sha256_16") != digest:
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def _gemm_fn(w):
+    from dense_gemm_sgemm_gb300 import gemm_hgemm_f16f32, gemm_sgemm_f32
+
+    return gemm_sgemm_f32 if w.dtype == "f32" else gemm_hgemm_f16f32
+
+
+def _device_inputs(w):
+    from dense_gemm_sgemm_gb300 import workloads
+
+    host = workloads.make_inputs(w)
+    return host, {k: v.cuda() for k, v in host.items()}
+
+
+def time_device(w, dev, steps, warmup, flush, barrier=None):
+    """Per-step CUDA-event times (ms) of the library call, L2 flushed before each step."""
+    import torch
+
+    fn = _gemm_fn(w)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, dev["A"], w.lda, dev["B"], w.ldb, w.beta,
+           dev["C"], w.ldc, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    wall0 = time.perf_counter()
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if barrier:
+        barrier()
+    return [s.elapsed_time(e) for s, e in ev], wall
+
+
+def time_e2e(w, host, dev, steps):
+    """Through the public API from pinned host buffers: H2D inputs, GEMM, D2H result."""
+    import torch
+
+    fn = _gemm_fn(w)
+    stream = torch.cuda.current_stream()
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out = torch.empty_like(pinned["C"]).pin_memory()
+    names = ["A", "B"] + (["C"] if w.beta != 0.0 else [])
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k in names:
+            dev[k].copy_(pinned[k], non_blocking=True)
+        fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, dev["A"], w.lda, dev["B"], w.ldb, w.beta,
+           dev["C"], w.ldc, stream)
+        out.copy_(dev["C"], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    e.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": round(w.flops / (ms * 1e-3) / 1e12, 4), "unit": UNIT,
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def oracle_sample(w, host, budget_s):
+    """Time the CPU oracle on a row slab of w sized to about budget_s seconds."""
+    import numpy as np
+
+    import oracle
+
+    A = host["A"].numpy()
+    B = host["B"].numpy()
+    if w.dtype == "f16":
+        A, B = A.view(np.uint16), B.view(np.uint16)
+    C = host["C"].numpy()
+    threads = oracle.default_threads()
+
+    def run(rows):
+        # rows of op(A) = N are contiguous rows of A; op(A) = T keeps every column block
+        if w.opA == "N":
+            a = A[:rows]
+        else:
+            a = A  # the oracle reads only the first `rows` columns through lda
+        t0 = time.perf_counter()
+        oracle.gemm(w.opA, w.opB, rows, w.N, w.K, w.alpha, a, w.lda, B, w.ldb, w.beta,
+                    C[:rows] if w.beta != 0.0 else None, w.ldc, dtype=w.dtype, threads=threads)
+        return time.perf_counter() - t0
+
+    probe = max(1, min(w.M, threads))
+    t = run(probe)
+    per_row = max(t / probe, 1e-7)
+    rows = int(max(probe, min(w.M, budget_s / per_row)))
+    return rows, threads, run
+
+
+# ------------------------------------------------------------------ the two arms
+def run_reference(args, rank, world):
+    from dense_gemm_sgemm_gb300 import workloads
+
+    if rank != 0:
+        return 0
+    w = workloads.by_name(args.workload)
+    host = workloads.make_inputs(w)
+    per_step_budget = max(0.01, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows, threads, run = oracle_sample(w, host, per_step_budget)
+    for _ in range(args.warmup):
+        run(rows)
+    times = [run(rows) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    flops = 2 * rows * w.N * w.K
+    val = flops / (ms * 1e-3) / 1e12
+    sample = f"rows 0..{rows - 1} of op(A) (of {w.M}) x full B, per step; fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "opA": w.opA, "opB": w.opB, "seed": w.seed},
+        "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import dense_gemm_sgemm_gb300 as lib
+    from dense_gemm_sgemm_gb300 import workloads
+
+    lib.load()  # fails loudly when the CUDA library is missing
+    torch.cuda.set_device(local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+    peaks = _peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    w = workloads.by_name(args.workload)
+    host, dev = _device_inputs(w)
+    clocks = ClockSampler(local)
+    clocks.start()
+    step_ms, wall = time_device(w, dev, args.steps, args.warmup, flush, barrier)
+    clk = clocks.stop()
+    status = lib.gemm_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {lib.gemm_status_string(status)}")
+    value, total_ms = whole_job_value(sum(step_ms), args.steps, w.flops, world,
+                                      torch.device("cuda", local))
+    mean_ms = statistics.fmean(step_ms)
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    if w.dtype == "f32":
+        kernel_src, kernel = "sgemm_ffma.cu", "sgemm_ffma"
+        bound, peak, peak_src = "alu", FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
+    else:
+        kernel_src, kernel = "hgemm_tcgen05.cu", "hgemm_tcgen05"
+        bound, peak = "tensor", peaks["bf16_tflops"]
+        peak_src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
+    traffic = _traffic_from_profile(kernel_src, f"{kernel}_{w.name}.txt")
+    vs = (round(value / (PAGES_RAGGED_GFLOPS / 1e3), 4)
+          if w.name == workloads.sgemm_ragged().name else None)
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": vs,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "opA": w.opA, "opB": w.opB, "seed": w.seed,
+                   "dist": f"A {w.dist_a}, B {w.dist_b}" + (f", C {w.dist_c}" if w.beta else ""),
+                   "l2": "flushed before every timed step (512 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 4),
+                     "peak": round(peak, 2), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": w.algorithmic_bytes, "peak_source": peak_src,
+                     "median_ms": round(statistics.median(step_ms), 5),
+                     "min_ms": round(min(step_ms), 5), "max_ms": round(max(step_ms), 5)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    e2e_steps = max(3, min(args.steps, 200))
+    line["e2e"] = time_e2e(w, host, dev, e2e_steps)
+    if rank == 0 and not args.no_suite:
+        line["suite"] = run_suite(peaks, flush)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows, threads, run = oracle_sample(w, host, 1.0)
+        reps = max(1, int(10.0 / max(run(rows), 1e-3)))
+        times = [run(rows) for _ in range(reps)]
+        cpu = 2 * rows * w.N * w.K / statistics.median(times) / 1e12
+        line["cpu_baseline"] = {"value": round(cpu, 6), "unit": UNIT, "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"rows 0..{rows - 1} of {w.M} (x full B), "
+                                          f"{reps} repetitions, median"}
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_suite(peaks, flush):
+    """The other headline shapes, timed like the main step (median of 20, L2 flushed)."""
+    import torch
+
+    from dense_gemm_sgemm_gb300 import workloads
+
+    out = []
+    fp16_peak = peaks["bf16_tflops"]  # fp16 and bf16 have the same nominal tensor rate
+    for w in (workloads.sgemm_cube(4096), workloads.sgemm_sweep(16384),
+              workloads.hgemm_square(4096), workloads.hgemm_square(8192), workloads.linear_fp16()):
+        host, dev = _device_inputs(w)
+        ms, _ = time_device(w, dev, 20, 5, flush)
+        med = statistics.median(ms)
+        tf = w.flops / (med * 1e-3) / 1e12
+        peak = FFMA_PEAK_TFLOPS if w.dtype == "f32" else fp16_peak
+        out.append({"workload": w.name, "dtype": w.dtype, "tflops": round(tf, 2),
+                    "median_ms": round(med, 4), "peak": round(peak, 1),
+                    "bound": "alu" if w.dtype == "f32" else "tensor",
+                    "frac": round(tf / peak, 4),
+                    "peak_source": ("152 SMs x 128 x 2 x 2.07 GHz" if w.dtype == "f32"
+                                    else f"bf16 burst ({peaks['source']}), fp16 same nominal rate")})
+        del host, dev
+        torch.cuda.empty_cache()
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sgemm_ragged_1001x777x513",
+                    help="workload of the timed step (names in dense_gemm_sgemm_gb300.workloads)")
+    ap.add_argument("--no-suite", action="store_true", help="skip the other headline shapes")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = _dist()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
