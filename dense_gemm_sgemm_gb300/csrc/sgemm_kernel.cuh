@@ -1,0 +1,600 @@
+// Strict-FP32 SGEMM on the CUDA cores of sm_103a: the kernel template.
+//
+// C = alpha * op(A) * op(B) + beta * C, row-major (copecc.github.io "GEMM" page, section
+// "核心问题与运算特征").  The kernel follows the blocking the pages build up, re-designed
+// for Blackwell:
+//   * block tile BM x BN, K sliced by BK and staged in shared memory (copecc "共享内存分块";
+//     ssxxe.cn section "2.1"), as a STAGES-deep cp.async ring instead of the pages'
+//     register double buffer (ssxxe.cn section "2.3") -- the copy engine fills slot s+3
+//     while the FMA units work on slot s, with one __syncthreads per K slice;
+//   * each thread owns a TM x TN outer-product tile split into 4 x 4 blocks spaced BM/2
+//     (BN/2) apart (copecc "二维寄存器分块"; ssxxe.cn section "2.2");
+//   * an operand keeps the orientation it has in global memory: rows that run along k
+//     (op(A) = T, op(B) = N) are staged as [k][m] and read with 128-bit loads (copecc
+//     "向量化访存"); rows that run along m or n (op(A) = N, op(B) = T) are staged as [m][k]
+//     and read as k pairs, so every copy is a straight 16-byte (aligned) or 4-byte
+//     (unaligned ld) cp.async and no copy transposes;
+//   * 16-byte chunk indices are XOR-swizzled (copecc "共享内存填充与重排", Swizzling) so the
+//     copies and the fragment reads hit distinct banks without padding;
+//   * the products are fused multiply-adds on packed fp32 pairs (fma.rn.f32x2 through
+//     __ffma2_rn), IEEE fp32 with round-to-nearest-even and no TF32;
+//   * ragged M, N and K are handled by zero-filled copies (cp.async src-size below the copy
+//     size) and predicated stores (yekq.top "LeetGPU 第二题", the 1001 x 513 x 777 case);
+//   * the 1-D grid is rasterised in groups of tile rows (copecc "线程块网格重排");
+//   * optionally K is split over gridDim.y CTAs whose partial tiles are summed in a fixed
+//     order by the last one to finish (deterministic split-K).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gemm_internal.h"
+
+namespace gemm {
+namespace sg {
+
+constexpr int kThreads = 256;
+
+// Operand staging modes: shared-memory orientation x copy width.
+constexpr int kMnVec = 0;     // stored rows run along k: stage [k][x], 16-byte copies
+constexpr int kMnScalar = 1;  // stored rows run along k: stage [k][x], 4-byte copies
+constexpr int kKVec = 2;      // stored rows run along x: stage [x][k], 16-byte copies
+constexpr int kKScalar = 3;   // stored rows run along x: stage [x][k], 4-byte copies
+constexpr int kKT = 4;        // stored rows run along x: stage [k][x], 4-byte copies that transpose
+__host__ __device__ constexpr bool is_k_major(int mode) { return mode == kKVec || mode == kKScalar; }
+
+struct SgemmParams {
+    int64_t M, N, K;
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+    float alpha, beta;
+    int64_t tiles_m, tiles_n;
+    int log_group;
+    int c_vec;  // C base 16-byte aligned and ldc % 4 == 0
+    // Split-K (gridDim.y = splits): split s sums k slices [s*kt_per_split, (s+1)*kt_per_split).
+    int splits, kt_per_split;
+    float *ws;               // splits x tiles partial tiles (splits > 1 only)
+    unsigned int *counters;  // one arrival counter per tile, zero between launches
+};
+
+template <int BM_, int BN_, int BK_, int TM_, int TN_, int STAGES_, int MIN_BLOCKS_>
+struct Cfg {
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_, STAGES = STAGES_;
+    static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+    static constexpr int TY = BM / TM, TX = BN / TN;  // thread grid
+    static constexpr int MB = TM / 4, NB = TN / 4;    // 4-wide blocks per thread
+    static constexpr int M_STRIDE = BM / MB, N_STRIDE = BN / NB;
+    static constexpr int A_STAGE = BK * BM, B_STAGE = BK * BN;  // floats per stage
+    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static_assert(TY * TX == kThreads, "one thread per TM x TN tile");
+    static_assert(TX % 8 == 0 && TY % 4 == 0, "a warp covers 4 x 8 threads");
+    static_assert(TM % 4 == 0 && TN % 4 == 0, "128-bit fragment loads");
+    static_assert(BM % 32 == 0 && BN % 32 == 0, "swizzle needs 8 chunks per [k][x] row");
+    static_assert(BK == 16, "[x][k] stages hold four 16-byte chunks per row");
+    static_assert(M_STRIDE % 16 == 0 && N_STRIDE % 16 == 0, "row swizzle repeats every 16 rows");
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Float offset of element (k, x) in a [BK][W] stage: 16-byte chunk index XOR (k mod 8).
+template <int W>
+__device__ __forceinline__ int swz_mn(int k, int x)
+{
+    return k * W + ((((x >> 2) ^ (k & 7)) << 2) | (x & 3));
+}
+
+// Float offset of element (x, k) in a [W][16] stage: chunk index (k / 4) XOR ((x / 4) mod 4).
+__device__ __forceinline__ int swz_k(int x, int k)
+{
+    return x * 16 + ((((k >> 2) ^ ((x >> 2) & 3)) << 2) | (k & 3));
+}
+
+// Copies BK x W slices of one operand into shared memory, one slice per call.  The
+// per-thread parts of every address (row, column, bank) are fixed at construction; a call
+// only adds the slice offset, so the unrolled copies use immediate offsets.
+//   X    stored matrix, ld its leading dimension (passed to load() from the parameters)
+//   ext  extent of the m (or n) dimension, x0 the tile origin along it
+template <int MODE, int W, int BK>
+struct SliceLoader;
+
+// Stored rows run along k, aligned: 16-byte copies into [k][x].
+template <int W, int BK>
+struct SliceLoader<kMnVec, W, BK> {
+    static constexpr int CPR = W / 4;              // 16-byte chunks per k row
+    static constexpr int R = BK * CPR / kThreads;  // copies per thread
+    static constexpr int KSTEP = kThreads / CPR;   // k distance between a thread's copies
+    static_assert(BK * CPR % kThreads == 0 && KSTEP % 8 == 0, "");
+    const float *p;   // element (kb, x) of slice 0
+    int kb;           // first k row of this thread
+    uint32_t bytes;   // valid bytes of this thread's chunk (ragged x tail)
+    uint32_t dst0;    // byte offset in a stage
+    __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
+    {
+        const int c = tid % CPR;
+        kb = tid / CPR;
+        const int64_t rem = ext - (x0 + 4 * c);
+        bytes = rem <= 0 ? 0u : (rem >= 4 ? 16u : static_cast<uint32_t>(rem * 4));
+        p = X + kb * ld + (bytes ? x0 + 4 * c : 0);
+        dst0 = static_cast<uint32_t>(kb * W + ((c ^ (kb & 7)) << 2)) * 4u;
+    }
+    __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
+                                         int64_t K) const
+    {
+        const float *q = p + k0 * ld;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = bytes && (k0 + kb + r * KSTEP < K);
+            cp_async16(stage + dst0 + r * KSTEP * W * 4, ok ? q + r * KSTEP * ld : base, ok ? bytes : 0u);
+        }
+    }
+};
+
+// Stored rows run along k, unaligned pointer or ld: 4-byte copies into [k][x].
+template <int W, int BK>
+struct SliceLoader<kMnScalar, W, BK> {
+    static constexpr int R = BK * W / kThreads;
+    static constexpr int KSTEP = kThreads / W;
+    static_assert(BK * W % kThreads == 0 && kThreads % W == 0, "");
+    const float *p;
+    int kb, x;
+    bool x_ok;
+    __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
+    {
+        x = tid % W;
+        kb = tid / W;
+        x_ok = x0 + x < ext;
+        p = X + kb * ld + (x_ok ? x0 + x : 0);
+    }
+    __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
+                                         int64_t K) const
+    {
+        const float *q = p + k0 * ld;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int k = kb + r * KSTEP;
+            const bool ok = x_ok && (k0 + k < K);
+            cp_async4(stage + static_cast<uint32_t>(swz_mn<W>(k, x)) * 4u, ok ? q + r * KSTEP * ld : base,
+                      ok ? 4u : 0u);
+        }
+    }
+};
+
+// Stored rows run along x (K contiguous), aligned: 16-byte copies into [x][k].  Four
+// consecutive threads take the four chunks of one 64-byte row.
+template <int W, int BK>
+struct SliceLoader<kKVec, W, BK> {
+    static constexpr int R = W * 4 / kThreads;  // rows per thread
+    static constexpr int XSTEP = kThreads / 4;   // row distance between a thread's copies
+    static_assert(W * 4 % kThreads == 0 && XSTEP % 16 == 0, "");
+    const float *p;   // element (x0 + xb, 4c) of X
+    int c4;           // first k of this thread's chunk
+    uint32_t row_ok;  // bit r: row xb + r * XSTEP inside the matrix
+    uint32_t dst0;
+    __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
+    {
+        const int xb = tid / 4;
+        c4 = 4 * (tid % 4);
+        row_ok = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (x0 + xb + r * XSTEP < ext) row_ok |= 1u << r;
+        p = X + (row_ok & 1u ? (x0 + xb) * ld : 0) + c4;
+        dst0 = static_cast<uint32_t>(swz_k(xb, c4)) * 4u;
+    }
+    __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
+                                         int64_t K) const
+    {
+        const int64_t rem = K - (k0 + c4);
+        const uint32_t bytes = rem <= 0 ? 0u : (rem >= 4 ? 16u : static_cast<uint32_t>(rem * 4));
+        const float *q = p + k0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = bytes && ((row_ok >> r) & 1u);
+            cp_async16(stage + dst0 + r * XSTEP * BK * 4, ok ? q + int64_t(r * XSTEP) * ld : base,
+                       ok ? bytes : 0u);
+        }
+    }
+};
+
+// Stored rows run along x, unaligned pointer or ld: 4-byte copies into [x][k], sixteen
+// consecutive threads per 64-byte row.
+template <int W, int BK>
+struct SliceLoader<kKScalar, W, BK> {
+    static constexpr int R = W * BK / kThreads;
+    static constexpr int XSTEP = kThreads / BK;
+    static_assert(W * BK % kThreads == 0 && XSTEP % 16 == 0, "");
+    const float *p;
+    int k;
+    uint32_t row_ok;
+    uint32_t dst0;
+    __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
+    {
+        const int xb = tid / BK;
+        k = tid % BK;
+        row_ok = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (x0 + xb + r * XSTEP < ext) row_ok |= 1u << r;
+        p = X + (row_ok & 1u ? (x0 + xb) * ld : 0) + k;
+        dst0 = static_cast<uint32_t>(swz_k(xb, k)) * 4u;
+    }
+    __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
+                                         int64_t K) const
+    {
+        const bool k_ok = k0 + k < K;
+        const float *q = p + k0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = k_ok && ((row_ok >> r) & 1u);
+            cp_async4(stage + dst0 + r * XSTEP * BK * 4, ok ? q + int64_t(r * XSTEP) * ld : base,
+                      ok ? 4u : 0u);
+        }
+    }
+};
+
+// Stored rows run along x, staged transposed as [k][x] with 4-byte copies.  Each warp
+// copies a 4 (x) by 8 (k) patch -- lanes 0-3 take four rows of X, lanes in steps of 4 walk
+// 8 consecutive k -- and the swizzle spreads its 32 stores over all 32 banks.  Costs more
+// copy instructions than a K-major stage but keeps the 128-bit fragment reads.
+template <int W, int BK>
+struct SliceLoader<kKT, W, BK> {
+    static constexpr int RX = W / 32;  // patches per thread along x
+    static constexpr int RK = BK / 8;  // patches per thread along k
+    static_assert(W % 32 == 0 && BK % 8 == 0 && kThreads == 256, "");
+    const float *p;   // element (x0 + xb, kb) of X
+    int kb;
+    uint32_t row_ok;  // bit i: row xb + 32 i inside the matrix
+    uint32_t dst0;
+    __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
+    {
+        const int lane = tid & 31, warp = tid >> 5;
+        const int xb = 4 * warp + (lane & 3);
+        kb = lane >> 2;
+        row_ok = 0;
+#pragma unroll
+        for (int i = 0; i < RX; ++i)
+            if (x0 + xb + 32 * i < ext) row_ok |= 1u << i;
+        p = X + (row_ok & 1u ? (x0 + xb) * ld : 0) + kb;
+        dst0 = static_cast<uint32_t>(kb * W + ((warp ^ kb) << 2) + (lane & 3)) * 4u;
+    }
+    __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
+                                         int64_t K) const
+    {
+        const float *q = p + k0;
+#pragma unroll
+        for (int rk = 0; rk < RK; ++rk) {
+            const bool k_ok = k0 + kb + 8 * rk < K;
+#pragma unroll
+            for (int rx = 0; rx < RX; ++rx) {
+                const bool ok = k_ok && ((row_ok >> rx) & 1u);
+                cp_async4(stage + dst0 + static_cast<uint32_t>(8 * rk * W + 32 * rx) * 4u,
+                          ok ? q + int64_t(32 * rx) * ld + 8 * rk : base, ok ? 4u : 0u);
+            }
+        }
+    }
+};
+
+// Fragment loads.  A thread's T values of an operand are 4-wide blocks STRIDE apart,
+// starting at row (or column) 4 * t4 of the tile.
+// [k][x] stages: the values at one k, two 128-bit loads per 8 values.
+template <int W, int T, int STRIDE>
+__device__ __forceinline__ void load_frag_mn(const float *stage, int k, int t4, float (&v)[T])
+{
+#pragma unroll
+    for (int b = 0; b < T / 4; ++b) {
+        const int c = (b * STRIDE) / 4 + t4;
+        const float4 f = *reinterpret_cast<const float4 *>(stage + k * W + ((c ^ (k & 7)) << 2));
+        v[4 * b + 0] = f.x; v[4 * b + 1] = f.y; v[4 * b + 2] = f.z; v[4 * b + 3] = f.w;
+    }
+}
+
+// [x][k] stages: the values at k and k+1 (k even: both in one 16-byte chunk), one 64-bit
+// load per row.
+template <int T, int STRIDE>
+__device__ __forceinline__ void load_frag_k_pair(const float *stage, int k, int t4, float (&v)[2][T])
+{
+#pragma unroll
+    for (int b = 0; b < T / 4; ++b)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int x = b * STRIDE + 4 * t4 + i;
+            const float2 f = *reinterpret_cast<const float2 *>(stage + swz_k(x, k));
+            v[0][4 * b + i] = f.x;
+            v[1][4 * b + i] = f.y;
+        }
+}
+
+template <class C, int A_MODE, int B_MODE, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(const SgemmParams p)
+{
+    extern __shared__ __align__(16) float smem[];
+    float *sA = smem;
+    float *sB = smem + C::STAGES * C::A_STAGE;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int ty = (warp / (C::TX / 8)) * 4 + (lane >> 3);
+    const int tx = (warp % (C::TX / 8)) * 8 + (lane & 7);
+
+    int64_t tm, tn;
+    raster(blockIdx.x, p.tiles_m, p.tiles_n, p.log_group, tm, tn);
+    const int64_t m0 = tm * C::BM, n0 = tn * C::BN;
+    const int KT_all = static_cast<int>((p.K + C::BK - 1) / C::BK);
+    const int split = SPLIT ? static_cast<int>(blockIdx.y) : 0;
+    const int kt0 = SPLIT ? split * p.kt_per_split : 0;
+    const int KT = SPLIT ? min(KT_all - kt0, p.kt_per_split) : KT_all;  // slices of this CTA
+
+    const uint32_t sA_addr = smem_addr(sA), sB_addr = smem_addr(sB);
+    const SliceLoader<A_MODE, C::BM, C::BK> la(p.A, p.lda, p.M, m0, tid);
+    const SliceLoader<B_MODE, C::BN, C::BK> lb(p.B, p.ldb, p.N, n0, tid);
+    auto load_tile = [&](int slot, int kt) {
+        const int64_t k0 = int64_t(kt0 + kt) * C::BK;
+        la.load(sA_addr + slot * C::A_STAGE * 4, p.A, p.lda, k0, p.K);
+        lb.load(sB_addr + slot * C::B_STAGE * 4, p.B, p.ldb, k0, p.K);
+    };
+
+#pragma unroll
+    for (int s = 0; s < C::STAGES - 1; ++s) {
+        if (s < KT) load_tile(s, s);
+        cp_async_commit();
+    }
+
+    // The epilogue reads C when beta != 0: ask L2 for this thread's rows now, so the reads
+    // at the end do not wait for DRAM.
+    if (p.beta != 0.0f && (!SPLIT || split == 0)) {
+#pragma unroll
+        for (int i = 0; i < C::TM; ++i) {
+            const int64_t gm = m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4);
+#pragma unroll
+            for (int jb = 0; jb < C::NB; ++jb) {
+                const int64_t gn = n0 + jb * C::N_STRIDE + tx * 4;
+                if (gm < p.M && gn < p.N) prefetch_l2(p.C + gm * p.ldc + gn);
+            }
+        }
+    }
+
+    float2 acc[C::TM][C::TN / 2];
+#pragma unroll
+    for (int i = 0; i < C::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < C::TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+    for (int kt = 0; kt < KT; ++kt) {
+        cp_async_wait<C::STAGES - 2>();
+        __syncthreads();  // slice kt is visible; every thread is done with slot (kt-1)
+        const int nt = kt + C::STAGES - 1;
+        if (nt < KT) load_tile(nt % C::STAGES, nt);
+        cp_async_commit();
+
+        const float *As = sA + (kt % C::STAGES) * C::A_STAGE;
+        const float *Bs = sB + (kt % C::STAGES) * C::B_STAGE;
+#pragma unroll
+        for (int k = 0; k < C::BK; k += 2) {
+            // K-major operands come in k pairs; [k][m] / [k][n] operands one k at a time.
+            float a2[2][C::TM], b2[2][C::TN];
+            if constexpr (is_k_major(A_MODE)) load_frag_k_pair<C::TM, C::M_STRIDE>(As, k, ty, a2);
+            if constexpr (is_k_major(B_MODE)) load_frag_k_pair<C::TN, C::N_STRIDE>(Bs, k, tx, b2);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                float a[C::TM], b[C::TN];
+                if constexpr (is_k_major(A_MODE)) {
+#pragma unroll
+                    for (int i = 0; i < C::TM; ++i) a[i] = a2[kk][i];
+                } else {
+                    load_frag_mn<C::BM, C::TM, C::M_STRIDE>(As, k + kk, ty, a);
+                }
+                if constexpr (is_k_major(B_MODE)) {
+#pragma unroll
+                    for (int j = 0; j < C::TN; ++j) b[j] = b2[kk][j];
+                } else {
+                    load_frag_mn<C::BN, C::TN, C::N_STRIDE>(Bs, k + kk, tx, b);
+                }
+#pragma unroll
+                for (int i = 0; i < C::TM; ++i) {
+                    const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < C::TN / 2; ++j)
+                        acc[i][j] = __ffma2_rn(ai, make_float2(b[2 * j], b[2 * j + 1]), acc[i][j]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    if constexpr (SPLIT) {
+        // Deterministic split-K: every split stores its partial tile, and the split that
+        // arrives last adds all partials in split order 0, 1, ..., splits-1 -- the same
+        // order whichever CTA finishes last -- before the epilogue.
+        constexpr int Q = C::TM * C::TN / 4;  // float4 per thread
+        constexpr int QR = C::TN / 4;         // float4 per accumulator row
+        const int64_t tile = blockIdx.x;
+        const int64_t tile4 = int64_t(C::BM) * C::BN / 4;
+        float4 *all = reinterpret_cast<float4 *>(p.ws) + tile * p.splits * tile4;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const float2 lo = acc[q / QR][2 * (q % QR)], hi = acc[q / QR][2 * (q % QR) + 1];
+            __stcg(all + split * tile4 + q * kThreads + tid, make_float4(lo.x, lo.y, hi.x, hi.y));
+        }
+        __threadfence();
+        __shared__ unsigned int s_last;
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned int prev = atomicAdd(p.counters + tile, 1u);
+            s_last = prev == static_cast<unsigned int>(p.splits - 1);
+            if (s_last) p.counters[tile] = 0;  // ready for the next launch
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        // One round per split, Q independent loads in flight per round.
+        for (int s2 = 0; s2 < p.splits; ++s2) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const float4 u = __ldcg(all + s2 * tile4 + q * kThreads + tid);
+                float2 &lo = acc[q / QR][2 * (q % QR)], &hi = acc[q / QR][2 * (q % QR) + 1];
+                if (s2 == 0) {
+                    lo = make_float2(u.x, u.y);
+                    hi = make_float2(u.z, u.w);
+                } else {
+                    lo.x += u.x; lo.y += u.y; hi.x += u.z; hi.y += u.w;
+                }
+            }
+        }
+    }
+
+    // Epilogue: C = alpha * acc + beta * C, beta == 0 never reads C.
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int i = 0; i < C::TM; ++i) {
+        const int64_t gm = m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4);
+        if (gm >= p.M) continue;
+        float *crow = p.C + gm * p.ldc;
+#pragma unroll
+        for (int jb = 0; jb < C::NB; ++jb) {
+            const int64_t gn = n0 + jb * C::N_STRIDE + tx * 4;
+            const float2 lo = acc[i][2 * jb], hi = acc[i][2 * jb + 1];
+            float v[4] = {lo.x, lo.y, hi.x, hi.y};
+            if (p.c_vec && gn + 3 < p.N) {
+                float4 o;
+                if (beta != 0.0f) {
+                    const float4 cin = *reinterpret_cast<const float4 *>(crow + gn);
+                    o.x = fmaf(alpha, v[0], beta * cin.x);
+                    o.y = fmaf(alpha, v[1], beta * cin.y);
+                    o.z = fmaf(alpha, v[2], beta * cin.z);
+                    o.w = fmaf(alpha, v[3], beta * cin.w);
+                } else {
+                    o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                }
+                *reinterpret_cast<float4 *>(crow + gn) = o;
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (gn + jj < p.N) {
+                        const float r = beta != 0.0f ? fmaf(alpha, v[jj], beta * crow[gn + jj])
+                                                     : alpha * v[jj];
+                        crow[gn + jj] = r;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <class C, bool SPLIT, int A_MODE, int B_MODE>
+cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
+{
+    auto kern = sgemm_ffma_kernel<C, A_MODE, B_MODE, SPLIT>;
+    // The shared-memory opt-in is a per-device function attribute: set it once per device.
+    static std::atomic<uint64_t> attr_set{0};
+    const uint64_t bit = uint64_t(1) << (dev_id & 63);
+    if (!(attr_set.load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit, std::memory_order_release);
+    }
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits));
+    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Staging of K-contiguous operands per tile configuration: the 8 x 8 thread tile keeps the
+// 128-bit [k][x] fragment reads (transposing copies, kKT); the 4 x 4 thread tile stages
+// [x][k] with straight copies (kKVec / kKScalar).
+template <class C>
+struct KContigModes {
+    static constexpr bool kTransposed = C::TM >= 8;
+};
+
+template <class C, bool SPLIT, int A_MODE>
+cudaError_t launch_b(int dev_id, int b_mode, const SgemmParams &p, cudaStream_t s)
+{
+    if constexpr (KContigModes<C>::kTransposed) {
+        switch (b_mode) {
+        case kMnVec: return launch_cfg<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
+        case kMnScalar: return launch_cfg<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
+        case kKT: return launch_cfg<C, SPLIT, A_MODE, kKT>(dev_id, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (b_mode) {
+        case kMnVec: return launch_cfg<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
+        case kMnScalar: return launch_cfg<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
+        case kKVec: return launch_cfg<C, SPLIT, A_MODE, kKVec>(dev_id, p, s);
+        case kKScalar: return launch_cfg<C, SPLIT, A_MODE, kKScalar>(dev_id, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+// Launches configuration C for the given staging modes.  p.tiles_m/tiles_n, p.splits and
+// p.kt_per_split must already describe the grid of C.
+template <class C, bool SPLIT>
+cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s)
+{
+    if constexpr (KContigModes<C>::kTransposed) {
+        switch (a_mode) {
+        case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
+        case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
+        case kKT: return launch_b<C, SPLIT, kKT>(dev_id, b_mode, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (a_mode) {
+        case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
+        case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
+        case kKVec: return launch_b<C, SPLIT, kKVec>(dev_id, b_mode, p, s);
+        case kKScalar: return launch_b<C, SPLIT, kKScalar>(dev_id, b_mode, p, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+// Tile configurations (one translation unit each, see sgemm_cfg_*.cu).
+using CfgL = Cfg<128, 128, 16, 8, 8, 4, 2>;  // 8 x 8 per thread, two CTAs per SM
+using CfgS = Cfg<64, 64, 16, 4, 4, 4, 3>;    // 4 x 4 per thread, three CTAs per SM
+static_assert(CfgL::BK == 16 && CfgS::BK == 16, "the host planner counts K in slices of 16");
+
+// Launchers defined in the configuration translation units.
+cudaError_t launch_L(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_LS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_S(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_SS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+
+}  // namespace sg
+}  // namespace gemm
