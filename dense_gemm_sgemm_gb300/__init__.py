@@ -16,6 +16,7 @@ from ._lib import GEMM_OP_N, GEMM_OP_T, STATUS, GemmError, library_path, load
 
 __all__ = [
     "GEMM_OP_N", "GEMM_OP_T", "GemmError", "gemm_sgemm_f32", "gemm_hgemm_f16f32",
+    "gemm_sgemm_f32_noalloc",
     "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
     "library_path", "load", "matmul",
 ]
@@ -76,6 +77,21 @@ def gemm_hgemm_f16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st
                                   lda, _addr(B, torch.float16), ldb, beta,
                                   _addr(C, torch.float32), ldc, _stream(stream))
     _check(st, "gemm_hgemm_f16f32")
+
+
+def gemm_sgemm_f32_noalloc(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """gemm_sgemm_f32 for callers that must not allocate device memory during the call.
+
+    The split-K scratch is a fixed 16 MiB + 16 KiB device array owned by the library (no
+    cudaMalloc ever); problems with more than 1024 tiles of 64 x 64 are refused
+    (GEMM_ERR_UNSUPPORTED), and calls that overlap on the GPU must not share the array.
+    """
+    import torch
+
+    st = load().gemm_sgemm_f32_noalloc(_op(opA), _op(opB), M, N, K, alpha, _addr(A, torch.float32),
+                                       lda, _addr(B, torch.float32), ldb, beta,
+                                       _addr(C, torch.float32), ldc, _stream(stream))
+    _check(st, "gemm_sgemm_f32_noalloc")
 
 
 def gemm_get_device_status(stream=None) -> int:

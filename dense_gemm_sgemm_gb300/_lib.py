@@ -31,6 +31,7 @@ _GEMM_ARGS = [_int, _int, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _v
 SIGNATURES = {
     "gemm_sgemm_f32": (_int, _GEMM_ARGS),
     "gemm_hgemm_f16f32": (_int, _GEMM_ARGS),
+    "gemm_sgemm_f32_noalloc": (_int, _GEMM_ARGS),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_status_string": (ctypes.c_char_p, [_int]),
     "gemm_version": (_int, []),

@@ -92,6 +92,33 @@ GEMM_API gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M
                                 int64_t ldc, void *stream);
 
 /*
+ * Allocation-free variant of gemm_sgemm_f32, for callers that must not allocate device
+ * memory while they run: a framework whose own allocator owns the device memory and
+ * forbids other cudaMalloc calls, or a latency-critical caller that cannot afford the
+ * blocking, device-wide synchronisation or late failure of an allocation.  The source
+ * pages have no counterpart to this entry point.
+ *
+ * Same arguments, rules and result as gemm_sgemm_f32 (strict FP32, row-major, caller-owned
+ * A, B, C), computed by the split-K kernel (64 x 64 tiles, K split over up to 16 CTAs whose
+ * partial tiles are added in a fixed order).  Its scratch -- arrival counters and partial
+ * tiles -- lives in one statically sized device array of 16 MiB + 16 KiB that the library
+ * holds on every GPU that loads it, until the process exits; the call itself never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Limit: ceil(M/64) * ceil(N/64) <= 1024 (the partial tiles of one split must fit 16 MiB);
+ * larger problems return GEMM_ERR_UNSUPPORTED without launching anything.
+ * The first call on a device looks up the device address of the scratch array (with that
+ * device current); make that first call before capturing the stream into a graph.
+ * Every call shares the one array, whose contents persist between calls: the call clears
+ * the counters it needs on `stream` before its kernel, but two calls whose work overlaps on
+ * the GPU (e.g. on different streams) race on the array and corrupt each other's results.
+ */
+GEMM_API gemm_status_t gemm_sgemm_f32_noalloc(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                              int64_t K, float alpha, const float *A, int64_t lda,
+                                              const float *B, int64_t ldb, float beta, float *C,
+                                              int64_t ldc, void *stream);
+
+/*
  * Waits for `stream`, then returns and clears the error word that kernels of this library
  * set on the current device when a bounded barrier wait expires (GEMM_ERR_DEVICE_TIMEOUT),
  * or GEMM_OK.  A kernel that sets the word leaves its output tile unwritten.
