@@ -10,7 +10,6 @@ import ctypes
 import os
 import threading
 
-from . import build as _build
 
 GEMM_OP_N = 0
 GEMM_OP_T = 1
@@ -51,6 +50,8 @@ class GemmError(RuntimeError):
 
 
 def library_path() -> str:
+    from . import build as _build
+
     return _build.LIB_PATH
 
 
@@ -65,6 +66,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             if not build_if_missing:
                 raise ImportError(
                     f"{path} is missing: build it with `python -m dense_gemm_sgemm_gb300.build`")
+            from . import build as _build
+
             _build.build()
         lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():

@@ -35,6 +35,17 @@ struct DeviceInfo {
 // Cached per-device properties of the current device; false if there is none.
 bool current_device(DeviceInfo &info);
 
+// Split-K workspace of one (device, stream): kWorkspaceBytes of partial tiles and
+// kWorkspaceCounters arrival counters that are zero between kernels.
+constexpr size_t kWorkspaceBytes = size_t(64) << 20;
+constexpr size_t kWorkspaceCounters = 8192;
+struct StreamWorkspace {
+    float *data = nullptr;
+    unsigned int *counters = nullptr;
+};
+// False when no workspace exists and none can be allocated now (e.g. during capture).
+bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out);
+
 // Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
 cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
                          int64_t K, float alpha, const float *A, int64_t lda, const float *B,

@@ -64,7 +64,28 @@ struct HgemmParams {
     int c_vec;               // C base 16-byte aligned and ldc % 4 == 0
     uint64_t timeout_ns;     // limit of every barrier wait
     int inject_stall;        // test hook: the producer never fills the first slice
+    // Work units.  Units [0, full_tiles) are whole 128 x 256 tiles.  When tail_halves is set,
+    // each tile of the last, partial wave becomes two units of 128 x 128 (left and right
+    // half), so twice as many SMs share that wave.  Every output element is still summed by
+    // one CTA over all of K in the same order, so the split changes no result bit.
+    int64_t full_tiles, num_units;
+    int tail_halves;
 };
+
+// Tile, column offset within it and width of work unit u.
+__device__ __forceinline__ void decode_unit(const HgemmParams &p, int64_t u, int64_t &t, int &n_off, int &width)
+{
+    if (u < p.full_tiles || !p.tail_halves) {
+        t = u;
+        n_off = 0;
+        width = BN;
+    } else {
+        const int64_t r = u - p.full_tiles;
+        t = p.full_tiles + (r >> 1);
+        n_off = static_cast<int>(r & 1) * (BN / 2);
+        width = BN / 2;
+    }
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -205,17 +226,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-9 and
 // 10-12 = 0), A/B major-ness in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in bits
 // 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn)
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn, int n = BN)
 {
     return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
-           (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+           (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ the kernel
 template <int A_MN, int B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const HgemmParams p)
+                     const __grid_constant__ CUtensorMap map_b_half, const HgemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -251,6 +272,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
+        tma_prefetch_desc(&map_b_half);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -273,10 +295,14 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per stage: a fill was issued / its parity
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int64_t tm, tn;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int64_t t, tm, tn;
+                int n_off, width;
+                decode_unit(p, u, t, n_off, width);
                 raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
-                const int32_t m0 = static_cast<int32_t>(tm * BM), n0 = static_cast<int32_t>(tn * BN);
+                const int32_t m0 = static_cast<int32_t>(tm * BM);
+                const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off;
+                const uint32_t bytes = A_STAGE_BYTES + uint32_t(width) * BK * 2;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
                         raise_abort(abort_flag);
@@ -284,10 +310,10 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_expect_tx(fb, STAGE_BYTES);
+                    mbar_expect_tx(fb, bytes);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    const bool stall = p.inject_stall && t == blockIdx.x && kb == 0;
+                    const bool stall = p.inject_stall && u == blockIdx.x && kb == 0;
                     if (!stall) {
                         const int32_t k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
@@ -298,11 +324,13 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
                             tma_load_2d(a_dst, &map_a, fb, k0, m0);
                         }
-                        if (B_MN) {  // B stored K x N: four 64 (n) x 64 (k) boxes
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0);
-                        } else {     // B stored N x K: one 64 (k) x 256 (n) box
+                        if (B_MN) {  // B stored K x N: width / 64 boxes of 64 (n) x 64 (k)
+                            for (int j = 0; j < width / 64; ++j)
+                                tma_load_2d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0);
+                        } else if (width == BN) {  // B stored N x K: one 64 (k) x 256 (n) box
                             tma_load_2d(b_dst, &map_b, fb, k0, n0);
+                        } else {     // half-width unit: one 64 (k) x 128 (n) box
+                            tma_load_2d(b_dst, &map_b_half, fb, k0, n0);
                         }
                     } else {
                         filled &= ~(1u << stage);  // nothing in flight on this slot
@@ -322,13 +350,18 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
+            constexpr uint32_t idesc_full = make_idesc(A_MN, B_MN, BN);
+            constexpr uint32_t idesc_half = make_idesc(A_MN, B_MN, BN / 2);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int64_t t;
+                int n_off, width;
+                decode_unit(p, u, t, n_off, width);
+                const uint32_t idesc = width == BN ? idesc_full : idesc_half;
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, tmo)) {
                     raise_abort(abort_flag);
                     break;
@@ -376,8 +409,10 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         int acc = 0;
         uint32_t acc_phase = 0;
         const float alpha = p.alpha, beta = p.beta;
-        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-            int64_t tm, tn;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            int64_t t, tm, tn;
+            int n_off, width;
+            decode_unit(p, u, t, n_off, width);
             raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
             if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo)) {
                 raise_abort(abort_flag);
@@ -389,11 +424,11 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             float *crow = p.C + (row_ok ? gm * p.ldc : 0);
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < width / 32; ++c) {
                 float v[32];
                 __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the predicated stores
                 tmem_ld_32(taddr + c * 32, v);
-                const int64_t gn0 = tn * BN + c * 32;
+                const int64_t gn0 = tn * BN + n_off + c * 32;
                 if (!row_ok || gn0 >= p.N) continue;
                 if (p.c_vec && gn0 + 32 <= p.N) {
 #pragma unroll
@@ -474,8 +509,8 @@ bool make_map(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t cols,
 }
 
 template <int A_MN, int B_MN>
-cudaError_t launch_t(int dev_id, int grid, const CUtensorMap &ma, const CUtensorMap &mb, const HgemmParams &p,
-                     cudaStream_t stream)
+cudaError_t launch_t(int dev_id, int grid, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
+                     const HgemmParams &p, cudaStream_t stream)
 {
     auto kern = hgemm_tcgen05_kernel<A_MN, B_MN>;
     static std::atomic<uint64_t> attr_set{0};
@@ -485,7 +520,7 @@ cudaError_t launch_t(int dev_id, int grid, const CUtensorMap &ma, const CUtensor
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit, std::memory_order_release);
     }
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, p);
+    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, mbh, p);
     return cudaGetLastError();
 }
 
@@ -498,10 +533,12 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, i
     if (dev.smem_optin < size_t(SMEM_BYTES)) return GEMM_ERR_NO_DEVICE;
     const int a_mn = opA == GEMM_OP_T;  // A stored K x M
     const int b_mn = opB == GEMM_OP_N;  // B stored K x N
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mbh;
     const bool ok_a = a_mn ? make_map(&ma, A, K, M, lda, 64, BK) : make_map(&ma, A, M, K, lda, BK, BM);
     const bool ok_b = b_mn ? make_map(&mb, B, K, N, ldb, 64, BK) : make_map(&mb, B, N, K, ldb, BK, BN);
-    if (!ok_a || !ok_b) return GEMM_ERR_MISALIGNED;
+    // half-width units of B stored N x K read 128 rows at a time
+    const bool ok_bh = b_mn ? make_map(&mbh, B, K, N, ldb, 64, BK) : make_map(&mbh, B, N, K, ldb, BK, BN / 2);
+    if (!ok_a || !ok_b || !ok_bh) return GEMM_ERR_MISALIGNED;
 
     HgemmParams p{};
     p.M = M; p.N = N; p.K = K;
@@ -519,10 +556,24 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, i
         p.timeout_ns = 20000000ull;
     }
     const int grid = static_cast<int>(p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms);
+    // Whole tiles for the full waves; when the last wave would leave more than half of the
+    // CTAs idle, its tiles are processed as two half-width units each.
+    p.full_tiles = p.num_tiles;
+    p.num_units = p.num_tiles;
+    p.tail_halves = 0;
+    {
+        const int64_t full = (p.num_tiles / grid) * grid, tail = p.num_tiles - full;
+        const char *e = std::getenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES");
+        if (tail > 0 && 2 * tail <= grid && !(e && e[0] == '1')) {
+            p.full_tiles = full;
+            p.num_units = full + 2 * tail;
+            p.tail_halves = 1;
+        }
+    }
 
     cudaError_t e;
-    if (a_mn) e = b_mn ? launch_t<1, 1>(dev.device, grid, ma, mb, p, stream) : launch_t<1, 0>(dev.device, grid, ma, mb, p, stream);
-    else e = b_mn ? launch_t<0, 1>(dev.device, grid, ma, mb, p, stream) : launch_t<0, 0>(dev.device, grid, ma, mb, p, stream);
+    if (a_mn) e = b_mn ? launch_t<1, 1>(dev.device, grid, ma, mb, mbh, p, stream) : launch_t<1, 0>(dev.device, grid, ma, mb, mbh, p, stream);
+    else e = b_mn ? launch_t<0, 1>(dev.device, grid, ma, mb, mbh, p, stream) : launch_t<0, 0>(dev.device, grid, ma, mb, mbh, p, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 

@@ -30,46 +30,8 @@ __global__ void scale_kernel(int64_t M, int64_t N, float beta, float *__restrict
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- split-K planning
-// Workspace of the split-K path: one per (device, stream), so that concurrent streams never
-// share partial tiles.  Allocated once, on the first call on that stream that splits, and
-// kept until the process exits; never allocated while the stream is being captured.
-constexpr size_t kWsBytes = size_t(64) << 20;
-constexpr size_t kWsCounters = 8192;
-
-struct SplitWorkspace {
-    float *ws = nullptr;
-    unsigned int *counters = nullptr;
-};
-
-std::mutex g_ws_mu;
-std::map<std::pair<int, cudaStream_t>, SplitWorkspace> g_ws;
-
-bool split_workspace(int dev, cudaStream_t stream, SplitWorkspace &out)
-{
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    auto it = g_ws.find({dev, stream});
-    if (it != g_ws.end()) {
-        out = it->second;
-        return true;
-    }
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-        cudaGetLastError();
-        return false;
-    }
-    SplitWorkspace w;
-    if (cudaMalloc(&w.ws, kWsBytes) != cudaSuccess ||
-        cudaMalloc(&w.counters, kWsCounters * sizeof(unsigned int)) != cudaSuccess ||
-        cudaMemset(w.counters, 0, kWsCounters * sizeof(unsigned int)) != cudaSuccess) {
-        cudaGetLastError();
-        if (w.ws) cudaFree(w.ws);
-        if (w.counters) cudaFree(w.counters);
-        return false;
-    }
-    g_ws[{dev, stream}] = w;
-    out = w;
-    return true;
-}
+constexpr size_t kWsBytes = kWorkspaceBytes;
+constexpr size_t kWsCounters = kWorkspaceCounters;
 
 // A launch plan: tile configuration ('L' = 128 x 128, 'S' = 64 x 64) and K splits.
 struct Plan {
@@ -129,8 +91,8 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     // 16-byte copies need a 16-byte aligned base and a leading dimension divisible by 4.
     const bool a_vec = aligned16(A) && lda % 4 == 0, b_vec = aligned16(B) && ldb % 4 == 0;
     Plan plan = choose_plan(M, N, K, dev.num_sms, true);
-    SplitWorkspace w;
-    if (plan.splits > 1 && !split_workspace(dev.device, stream, w))
+    StreamWorkspace w;
+    if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
         plan = choose_plan(M, N, K, dev.num_sms, false);  // no workspace: plan without split
     const int bm = plan.cfg == 'L' ? CfgL::BM : CfgS::BM, bn = plan.cfg == 'L' ? CfgL::BN : CfgS::BN;
     const int KT = static_cast<int>((K + 15) / 16);
@@ -144,7 +106,7 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     p.splits = plan.splits;
     p.kt_per_split = (KT + plan.splits - 1) / plan.splits;
     if (plan.splits > 1) {
-        p.ws = w.ws;
+        p.ws = w.data;
         p.counters = w.counters;
         return plan.cfg == 'L' ? launch_LS(dev.device, a_mode, b_mode, p, stream)
                                : launch_SS(dev.device, a_mode, b_mode, p, stream);

@@ -1,0 +1,49 @@
+// Per-(device, stream) workspace of the split-K paths of both kernels.
+//
+// One workspace per (device, stream): calls on the same stream are ordered and may share it;
+// calls on different streams never do.  It is allocated once, on the first call on that
+// stream that splits K, kept until the process exits, and never allocated while the stream
+// is being captured (the call then runs without splitting).  Every kernel that uses the
+// arrival counters leaves them at zero when it finishes.
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gemm_internal.h"
+
+namespace gemm {
+namespace {
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, StreamWorkspace> g_ws;
+}  // namespace
+
+bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out)
+{
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws.find({dev, stream});
+    if (it != g_ws.end()) {
+        out = it->second;
+        return true;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return false;
+    }
+    StreamWorkspace w;
+    if (cudaMalloc(&w.data, kWorkspaceBytes) != cudaSuccess ||
+        cudaMalloc(&w.counters, kWorkspaceCounters * sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemset(w.counters, 0, kWorkspaceCounters * sizeof(unsigned int)) != cudaSuccess) {
+        cudaGetLastError();
+        if (w.data) cudaFree(w.data);
+        if (w.counters) cudaFree(w.counters);
+        return false;
+    }
+    g_ws[{dev, stream}] = w;
+    out = w;
+    return true;
+}
+
+}  // namespace gemm

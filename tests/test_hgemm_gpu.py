@@ -114,3 +114,33 @@ def test_beta_zero_ignores_nan():
     gemm_hgemm_f16f32("N", "N", M, N, K, 1.0, A, K, B, N, 0.0, C, N)
     torch.cuda.synchronize()
     assert torch.isfinite(C).all()
+
+
+def test_tail_wave_half_width_units_full_oracle():
+    # 18 x 10 = 180 tiles of 128 x 256: 152 run whole, and each of the 28 tiles of the last
+    # wave runs as two 128 x 128 units on different SMs.
+    w = workloads.Workload("hgemm_tail_2300x2560x512", "f16", 2300, 2560, 512, alpha=0.75,
+                           beta=0.5, seed=12, pad=(0, 0, 3))
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"][:, : w.N].contiguous())
+    assert torch.isnan(dev["C"][:, w.N:]).all()
+
+
+@pytest.mark.parametrize("opB", ["N", "T"])
+def test_tail_wave_half_width_units_integer_bit_exact(opB):
+    w = workloads.Workload(f"hgemm_tail_int_{opB}", "f16", 2304, 2600, 512, opB=opB, seed=13,
+                           dist_a="int4", dist_b="int4", pad=(0, (-2600) % 8 if opB == "N" else 0, 0))
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"], integer=True)
+
+
+def test_tail_half_units_change_no_bit(monkeypatch):
+    # Each output element is summed by one CTA over all of K either way.
+    w = workloads.Workload("hgemm_tail_same_bits", "f16", 2304, 2560, 640, seed=14)
+    inputs, dev = _run(w)
+    with_halves = dev["C"].clone()
+    monkeypatch.setenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES", "1")
+    dev["C"].copy_(inputs["C"].cuda())
+    parity.run_library(w, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(with_halves.view(torch.int32), dev["C"].view(torch.int32))
