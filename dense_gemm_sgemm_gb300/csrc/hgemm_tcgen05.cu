@@ -161,6 +161,44 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Multicast load: the box lands at the same shared-memory offset in every CTA of the cluster
+// named in cta_mask, and each of them gets the complete_tx on its barrier at offset `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                               int32_t c0, int32_t c1, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -186,6 +224,16 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// The same, arriving on the barrier at offset `bar` in every CTA of cta_mask.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -233,10 +281,15 @@ __host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn, int n = BN
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int A_MN, int B_MN>
+// MC = false: one CTA per tile.  MC = true: clusters of two CTAs along M share the B tile --
+// each loads its own A and half of B, multicasting that half to both CTAs, so each SM's
+// tensor-memory-access unit moves 32 KB instead of 48 KB per K slice.  Units then count
+// tile pairs: the CTA of cluster rank r computes tile row 2 * pair_row + r.
+template <int A_MN, int B_MN, bool MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_b_half, const HgemmParams p)
+                     const __grid_constant__ CUtensorMap map_b_half,
+                     const __grid_constant__ CUtensorMap map_b_quarter, const HgemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -258,10 +311,18 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Unit schedule: CTAs (or clusters) stride over the units; the raster runs over tiles
+    // (or tile pairs along M).
+    const int rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+    const int64_t unit0 = MC ? int64_t(cluster_id_x()) : int64_t(blockIdx.x);
+    const int64_t ustride = MC ? int64_t(cluster_count_x()) : int64_t(gridDim.x);
+    const int64_t rows_r = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
+    constexpr uint16_t kPair = 0x3;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC ? 2 : 1);  // MC: both CTAs' MMAs release a slot
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -273,6 +334,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
         tma_prefetch_desc(&map_b_half);
+        if (MC) tma_prefetch_desc(&map_b_quarter);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -283,6 +345,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     }
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();  // the peer's barriers exist before any multicast targets them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -295,11 +358,12 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per stage: a fill was issued / its parity
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
                 int64_t t, tm, tn;
                 int n_off, width;
                 decode_unit(p, u, t, n_off, width);
-                raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
+                raster(t, rows_r, p.tiles_n, kLogGroup, tm, tn);
+                if (MC) tm = 2 * tm + rank;
                 const int32_t m0 = static_cast<int32_t>(tm * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off;
                 const uint32_t bytes = A_STAGE_BYTES + uint32_t(width) * BK * 2;
@@ -313,7 +377,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     mbar_expect_tx(fb, bytes);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    const bool stall = p.inject_stall && u == blockIdx.x && kb == 0;
+                    const bool stall = p.inject_stall && u == unit0 && kb == 0;
                     if (!stall) {
                         const int32_t k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
@@ -324,7 +388,18 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
                             tma_load_2d(a_dst, &map_a, fb, k0, m0);
                         }
-                        if (B_MN) {  // B stored K x N: width / 64 boxes of 64 (n) x 64 (k)
+                        if (MC) {
+                            // This CTA's half of the unit's B columns, multicast to both CTAs.
+                            const int half = width / 2;
+                            const int32_t nb = n0 + rank * half;
+                            const uint32_t bd = b_dst + uint32_t(rank) * uint32_t(half) * 128u;
+                            if (B_MN) {
+                                for (int j = 0; j < half / 64; ++j)
+                                    tma_load_2d_mc(bd + 8192 * j, &map_b, fb, nb + 64 * j, k0, kPair);
+                            } else {
+                                tma_load_2d_mc(bd, half == BN / 2 ? &map_b_half : &map_b_quarter, fb, k0, nb, kPair);
+                            }
+                        } else if (B_MN) {  // B stored K x N: width / 64 boxes of 64 (n) x 64 (k)
                             for (int j = 0; j < width / 64; ++j)
                                 tma_load_2d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0);
                         } else if (width == BN) {  // B stored N x K: one 64 (k) x 256 (n) box
@@ -345,6 +420,16 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         const volatile int no_abort = 0;
                         mbar_wait(full_bar(s), (fill_parity >> s) & 1u, &no_abort, 100000000ull);
                     }
+            } else if (MC) {
+                // Wait for the last release of every slot by both CTAs' MMAs, so that no
+                // arrival from the peer is still on its way when this CTA exits.
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
+                        raise_abort(abort_flag);
+                        break;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
             }
         }
     } else if (warp == 1) {
@@ -357,7 +442,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
                 int64_t t;
                 int n_off, width;
                 decode_unit(p, u, t, n_off, width);
@@ -388,7 +473,9 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
-                    umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
+                    // slot free once these MMAs have read it (MC: in both CTAs' counts)
+                    if (MC) umma_commit_mc(empty_bar(stage), kPair);
+                    else umma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -409,11 +496,12 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         int acc = 0;
         uint32_t acc_phase = 0;
         const float alpha = p.alpha, beta = p.beta;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        for (int64_t u = unit0; u < p.num_units; u += ustride) {
             int64_t t, tm, tn;
             int n_off, width;
             decode_unit(p, u, t, n_off, width);
-            raster(t, p.tiles_m, p.tiles_n, kLogGroup, tm, tn);
+            raster(t, rows_r, p.tiles_n, kLogGroup, tm, tn);
+            if (MC) tm = 2 * tm + rank;
             if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo)) {
                 raise_abort(abort_flag);
                 break;
@@ -467,6 +555,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();  // neither CTA leaves while the other may still signal it
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
@@ -508,20 +597,98 @@ bool make_map(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t cols,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+struct Maps {
+    CUtensorMap a, b, b_half, b_quarter;
+};
+
+// Largest number of two-CTA clusters of this kernel that can be resident at once (0: none).
 template <int A_MN, int B_MN>
-cudaError_t launch_t(int dev_id, int grid, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
-                     const HgemmParams &p, cudaStream_t stream)
+int max_pair_clusters(int dev_id)
 {
-    auto kern = hgemm_tcgen05_kernel<A_MN, B_MN>;
+    static std::atomic<int> cached[64];
+    static std::atomic<uint64_t> known{0};
+    const uint64_t bit = uint64_t(1) << (dev_id & 63);
+    if (known.load(std::memory_order_acquire) & bit) return cached[dev_id & 63].load();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tcgen05_kernel<A_MN, B_MN, true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cached[dev_id & 63].store(n);
+    known.fetch_or(bit, std::memory_order_release);
+    return n;
+}
+
+template <int A_MN, int B_MN, bool MC>
+cudaError_t set_smem_attr(int dev_id)
+{
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = uint64_t(1) << (dev_id & 63);
-    if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set.fetch_or(bit, std::memory_order_release);
+    if (attr_set.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, MC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// Plans the unit schedule and launches.  With clusters, units are tile pairs along M.
+template <int A_MN, int B_MN>
+cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaStream_t stream)
+{
+    const char *no_mc = std::getenv("GEMM_GB300_HGEMM_NO_MULTICAST");
+    const char *no_halves = std::getenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES");
+    bool mc = p.tiles_m >= 2 && !(no_mc && no_mc[0] == '1');
+    int max_clusters = 0;
+    if (mc) {
+        if (set_smem_attr<A_MN, B_MN, true>(dev.device) != cudaSuccess) return cudaGetLastError();
+        max_clusters = max_pair_clusters<A_MN, B_MN>(dev.device);
+        mc = max_clusters > 0;
     }
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, mbh, p);
-    return cudaGetLastError();
+    // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
+    // half of the workers idle, its tiles are processed as two half-width units each.
+    const int64_t work = mc ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
+    const int64_t workers_max = mc ? max_clusters : dev.num_sms;
+    const int64_t workers = work < workers_max ? work : workers_max;
+    p.full_tiles = work;
+    p.num_units = work;
+    p.tail_halves = 0;
+    const int64_t full = (work / workers) * workers, tail = work - full;
+    if (tail > 0 && 2 * tail <= workers && !(no_halves && no_halves[0] == '1')) {
+        p.full_tiles = full;
+        p.num_units = full + 2 * tail;
+        p.tail_halves = 1;
+    }
+    if (!mc) {
+        cudaError_t e = set_smem_attr<A_MN, B_MN, false>(dev.device);
+        if (e != cudaSuccess) return e;
+        hgemm_tcgen05_kernel<A_MN, B_MN, false><<<static_cast<unsigned>(workers), kThreads, SMEM_BYTES, stream>>>(
+            m.a, m.b, m.b_half, m.b_quarter, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * workers), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true>, m.a, m.b, m.b_half, m.b_quarter, p);
 }
 
 }  // namespace
@@ -533,12 +700,18 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, i
     if (dev.smem_optin < size_t(SMEM_BYTES)) return GEMM_ERR_NO_DEVICE;
     const int a_mn = opA == GEMM_OP_T;  // A stored K x M
     const int b_mn = opB == GEMM_OP_N;  // B stored K x N
-    CUtensorMap ma, mb, mbh;
-    const bool ok_a = a_mn ? make_map(&ma, A, K, M, lda, 64, BK) : make_map(&ma, A, M, K, lda, BK, BM);
-    const bool ok_b = b_mn ? make_map(&mb, B, K, N, ldb, 64, BK) : make_map(&mb, B, N, K, ldb, BK, BN);
-    // half-width units of B stored N x K read 128 rows at a time
-    const bool ok_bh = b_mn ? make_map(&mbh, B, K, N, ldb, 64, BK) : make_map(&mbh, B, N, K, ldb, BK, BN / 2);
-    if (!ok_a || !ok_b || !ok_bh) return GEMM_ERR_MISALIGNED;
+    Maps m;
+    const bool ok_a = a_mn ? make_map(&m.a, A, K, M, lda, 64, BK) : make_map(&m.a, A, M, K, lda, BK, BM);
+    bool ok_b;
+    if (b_mn) {  // 64 (n) x 64 (k) boxes serve every unit width
+        ok_b = make_map(&m.b, B, K, N, ldb, 64, BK);
+        m.b_half = m.b;
+        m.b_quarter = m.b;
+    } else {     // B stored N x K: boxes of 256, 128 and 64 rows
+        ok_b = make_map(&m.b, B, N, K, ldb, BK, BN) && make_map(&m.b_half, B, N, K, ldb, BK, BN / 2) &&
+               make_map(&m.b_quarter, B, N, K, ldb, BK, BN / 4);
+    }
+    if (!ok_a || !ok_b) return GEMM_ERR_MISALIGNED;
 
     HgemmParams p{};
     p.M = M; p.N = N; p.K = K;
@@ -555,25 +728,9 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, i
         p.inject_stall = 1;
         p.timeout_ns = 20000000ull;
     }
-    const int grid = static_cast<int>(p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms);
-    // Whole tiles for the full waves; when the last wave would leave more than half of the
-    // CTAs idle, its tiles are processed as two half-width units each.
-    p.full_tiles = p.num_tiles;
-    p.num_units = p.num_tiles;
-    p.tail_halves = 0;
-    {
-        const int64_t full = (p.num_tiles / grid) * grid, tail = p.num_tiles - full;
-        const char *e = std::getenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES");
-        if (tail > 0 && 2 * tail <= grid && !(e && e[0] == '1')) {
-            p.full_tiles = full;
-            p.num_units = full + 2 * tail;
-            p.tail_halves = 1;
-        }
-    }
-
     cudaError_t e;
-    if (a_mn) e = b_mn ? launch_t<1, 1>(dev.device, grid, ma, mb, mbh, p, stream) : launch_t<1, 0>(dev.device, grid, ma, mb, mbh, p, stream);
-    else e = b_mn ? launch_t<0, 1>(dev.device, grid, ma, mb, mbh, p, stream) : launch_t<0, 0>(dev.device, grid, ma, mb, mbh, p, stream);
+    if (a_mn) e = b_mn ? launch_t<1, 1>(dev, m, p, stream) : launch_t<1, 0>(dev, m, p, stream);
+    else e = b_mn ? launch_t<0, 1>(dev, m, p, stream) : launch_t<0, 0>(dev, m, p, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
