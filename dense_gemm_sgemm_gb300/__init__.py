@@ -7,6 +7,9 @@ in the library's CUDA kernels; torch only owns the memory and the stream.
 
     gemm_sgemm_f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
     gemm_hgemm_f16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+    gemm_bgemm_bf16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+    gemm_*_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                           beta, C, ldc, strideC, batch)
 """
 from __future__ import annotations
 
@@ -16,7 +19,8 @@ from ._lib import GEMM_OP_N, GEMM_OP_T, STATUS, GemmError, library_path, load
 
 __all__ = [
     "GEMM_OP_N", "GEMM_OP_T", "GemmError", "gemm_sgemm_f32", "gemm_hgemm_f16f32",
-    "gemm_sgemm_f32_noalloc",
+    "gemm_bgemm_bf16f32", "gemm_sgemm_f32_strided_batched", "gemm_hgemm_f16f32_strided_batched",
+    "gemm_bgemm_bf16f32_strided_batched", "gemm_sgemm_f32_noalloc",
     "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
     "library_path", "load", "matmul",
 ]
@@ -77,6 +81,52 @@ def gemm_hgemm_f16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st
                                   lda, _addr(B, torch.float16), ldb, beta,
                                   _addr(C, torch.float32), ldc, _stream(stream))
     _check(st, "gemm_hgemm_f16f32")
+
+
+def gemm_bgemm_bf16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    import torch
+
+    st = load().gemm_bgemm_bf16f32(_op(opA), _op(opB), M, N, K, alpha, _addr(A, torch.bfloat16),
+                                   lda, _addr(B, torch.bfloat16), ldb, beta,
+                                   _addr(C, torch.float32), ldc, _stream(stream))
+    _check(st, "gemm_bgemm_bf16f32")
+
+
+_BATCHED = {
+    "f32": ("gemm_sgemm_f32_strided_batched", "float32"),
+    "f16": ("gemm_hgemm_f16f32_strided_batched", "float16"),
+    "bf16": ("gemm_bgemm_bf16f32_strided_batched", "bfloat16"),
+}
+
+
+def _batched(kind, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+             strideC, batch, stream):
+    import torch
+
+    name, dt = _BATCHED[kind]
+    dt = getattr(torch, dt)
+    st = getattr(load(), name)(_op(opA), _op(opB), M, N, K, alpha, _addr(A, dt), lda, strideA,
+                               _addr(B, dt), ldb, strideB, beta, _addr(C, torch.float32), ldc,
+                               strideC, batch, _stream(stream))
+    _check(st, name)
+
+
+def gemm_sgemm_f32_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                                   beta, C, ldc, strideC, batch, stream=None):
+    _batched("f32", opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+             strideC, batch, stream)
+
+
+def gemm_hgemm_f16f32_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                                      beta, C, ldc, strideC, batch, stream=None):
+    _batched("f16", opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+             strideC, batch, stream)
+
+
+def gemm_bgemm_bf16f32_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb,
+                                       strideB, beta, C, ldc, strideC, batch, stream=None):
+    _batched("bf16", opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+             strideC, batch, stream)
 
 
 def gemm_sgemm_f32_noalloc(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
@@ -140,7 +190,8 @@ def matmul(A, B, C=None, alpha=1.0, beta=0.0, opA="N", opB="N", stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if C.shape != (M, N) or C.stride(1) != 1 or C.dtype != torch.float32:
         raise ValueError("C must be fp32, M x N, unit column stride")
-    fn = gemm_sgemm_f32 if A.dtype == torch.float32 else gemm_hgemm_f16f32
+    fn = {torch.float32: gemm_sgemm_f32, torch.float16: gemm_hgemm_f16f32,
+          torch.bfloat16: gemm_bgemm_bf16f32}[A.dtype]
     fn(opA, opB, M, N, K, alpha, A, max(A.stride(0), 1), B, max(B.stride(0), 1), beta, C,
        max(C.stride(0), 1), stream)
     return C

@@ -27,9 +27,15 @@ STATUS = {
 # Every symbol include/gemm_gb300.h declares, with (restype, argtypes).
 _i64, _f32, _int, _vp = ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_void_p
 _GEMM_ARGS = [_int, _int, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]
+_BATCHED_ARGS = [_int, _int, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64, _i64, _f32, _vp,
+                 _i64, _i64, _i64, _vp]
 SIGNATURES = {
     "gemm_sgemm_f32": (_int, _GEMM_ARGS),
     "gemm_hgemm_f16f32": (_int, _GEMM_ARGS),
+    "gemm_bgemm_bf16f32": (_int, _GEMM_ARGS),
+    "gemm_sgemm_f32_strided_batched": (_int, _BATCHED_ARGS),
+    "gemm_hgemm_f16f32_strided_batched": (_int, _BATCHED_ARGS),
+    "gemm_bgemm_bf16f32_strided_batched": (_int, _BATCHED_ARGS),
     "gemm_sgemm_f32_noalloc": (_int, _GEMM_ARGS),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_status_string": (ctypes.c_char_p, [_int]),

@@ -75,15 +75,29 @@ static gemm_status_t from_cuda(cudaError_t e)
 
 using namespace gemm;
 
-extern "C" {
+namespace gemm {
 
-gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
-                             float alpha, const float *A, int64_t lda, const float *B,
-                             int64_t ldb, float beta, float *C, int64_t ldc, void *stream)
+// Batch rules shared by every strided-batched call: batch >= 0, strides >= 0, and the
+// outputs of different problems must not overlap (strideC covers one M x N matrix).
+static gemm_status_t check_batch(int64_t M, int64_t N, int64_t ldc, int64_t strideA, int64_t strideB,
+                                 int64_t strideC, int64_t batch)
+{
+    if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return GEMM_ERR_INVALID_VALUE;
+    if (batch > 1 && M > 0 && N > 0 && strideC < (M - 1) * ldc + N) return GEMM_ERR_INVALID_VALUE;
+    if (batch > (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;
+}
+
+static gemm_status_t sgemm_impl(int opA, int opB, int64_t M, int64_t N, int64_t K, float alpha,
+                                const float *A, int64_t lda, int64_t strideA, const float *B,
+                                int64_t ldb, int64_t strideB, float beta, float *C, int64_t ldc,
+                                int64_t strideC, int64_t batch, void *stream)
 {
     const bool need_ab = K > 0 && alpha != 0.0f;
     gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
-    if (s != GEMM_OK || M == 0 || N == 0) return s;
+    if (s != GEMM_OK) return s;
+    s = check_batch(M, N, ldc, strideA, strideB, strideC, batch);
+    if (s != GEMM_OK || M == 0 || N == 0 || batch == 0) return s;
     if (!aligned(C, 4) || (need_ab && (!aligned(A, 4) || !aligned(B, 4))))
         return GEMM_ERR_MISALIGNED;
     DeviceInfo dev;
@@ -91,9 +105,59 @@ gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!need_ab) {
         if (beta == 1.0f) return GEMM_OK;
-        return from_cuda(launch_scale(M, N, beta, C, ldc, st));
+        return from_cuda(launch_scale_batched(M, N, beta, C, ldc, strideC, batch, st));
     }
-    return from_cuda(launch_sgemm(dev, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st));
+    return from_cuda(launch_sgemm(dev, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+                                  ldc, strideC, batch, st));
+}
+
+static gemm_status_t tc_impl(int dtype, int opA, int opB, int64_t M, int64_t N, int64_t K, float alpha,
+                             const uint16_t *A, int64_t lda, int64_t strideA, const uint16_t *B,
+                             int64_t ldb, int64_t strideB, float beta, float *C, int64_t ldc,
+                             int64_t strideC, int64_t batch, void *stream)
+{
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
+    if (s != GEMM_OK) return s;
+    s = check_batch(M, N, ldc, strideA, strideB, strideC, batch);
+    if (s != GEMM_OK || M == 0 || N == 0 || batch == 0) return s;
+    if (!aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    if (need_ab && (!aligned(A, 16) || !aligned(B, 16) || (lda % 8) != 0 || (ldb % 8) != 0))
+        return GEMM_ERR_MISALIGNED;
+    if (need_ab && batch > 1 && ((strideA % 8) != 0 || (strideB % 8) != 0)) return GEMM_ERR_MISALIGNED;
+    if (need_ab && (lda > (int64_t(1) << 35) || ldb > (int64_t(1) << 35) || strideA > (int64_t(1) << 38) ||
+                    strideB > (int64_t(1) << 38)))
+        return GEMM_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!need_ab) {
+        if (beta == 1.0f) return GEMM_OK;
+        return from_cuda(launch_scale_batched(M, N, beta, C, ldc, strideC, batch, st));
+    }
+    return launch_hgemm(dev, dtype, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                        strideC, batch, st);
+}
+
+}  // namespace gemm
+
+extern "C" {
+
+gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float beta, float *C, int64_t ldc, void *stream)
+{
+    return sgemm_impl(opA, opB, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, stream);
+}
+
+gemm_status_t gemm_sgemm_f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                             int64_t K, float alpha, const float *A, int64_t lda,
+                                             int64_t strideA, const float *B, int64_t ldb,
+                                             int64_t strideB, float beta, float *C, int64_t ldc,
+                                             int64_t strideC, int64_t batch, void *stream)
+{
+    return sgemm_impl(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+                      batch, stream);
 }
 
 gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
@@ -101,22 +165,34 @@ gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t
                                 const uint16_t *B, int64_t ldb, float beta, float *C,
                                 int64_t ldc, void *stream)
 {
-    const bool need_ab = K > 0 && alpha != 0.0f;
-    gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
-    if (s != GEMM_OK || M == 0 || N == 0) return s;
-    if (!aligned(C, 4)) return GEMM_ERR_MISALIGNED;
-    if (need_ab && (!aligned(A, 16) || !aligned(B, 16) || (lda % 8) != 0 || (ldb % 8) != 0))
-        return GEMM_ERR_MISALIGNED;
-    if (need_ab && (lda > (int64_t(1) << 35) || ldb > (int64_t(1) << 35)))
-        return GEMM_ERR_UNSUPPORTED;
-    DeviceInfo dev;
-    if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (!need_ab) {
-        if (beta == 1.0f) return GEMM_OK;
-        return from_cuda(launch_scale(M, N, beta, C, ldc, st));
-    }
-    return launch_hgemm(dev, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, st);
+    return tc_impl(kInF16, opA, opB, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, stream);
+}
+
+gemm_status_t gemm_hgemm_f16f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                                int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                                int64_t strideA, const uint16_t *B, int64_t ldb,
+                                                int64_t strideB, float beta, float *C, int64_t ldc,
+                                                int64_t strideC, int64_t batch, void *stream)
+{
+    return tc_impl(kInF16, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+                   batch, stream);
+}
+
+gemm_status_t gemm_bgemm_bf16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const uint16_t *A, int64_t lda, const uint16_t *B,
+                                 int64_t ldb, float beta, float *C, int64_t ldc, void *stream)
+{
+    return tc_impl(kInBf16, opA, opB, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, stream);
+}
+
+gemm_status_t gemm_bgemm_bf16f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                                 int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                                 int64_t strideA, const uint16_t *B, int64_t ldb,
+                                                 int64_t strideB, float beta, float *C, int64_t ldc,
+                                                 int64_t strideC, int64_t batch, void *stream)
+{
+    return tc_impl(kInBf16, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                   strideC, batch, stream);
 }
 
 gemm_status_t gemm_get_device_status(void *stream)

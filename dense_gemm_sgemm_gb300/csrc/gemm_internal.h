@@ -47,18 +47,30 @@ struct StreamWorkspace {
 bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out);
 
 // Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
+// A batch of `batch` problems: operand b of problem i starts `stride` elements after that
+// of problem i-1 (stride 0: all problems share the operand).
 cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
-                         int64_t K, float alpha, const float *A, int64_t lda, const float *B,
-                         int64_t ldb, float beta, float *C, int64_t ldc, cudaStream_t stream);
+                         int64_t K, float alpha, const float *A, int64_t lda, int64_t strideA,
+                         const float *B, int64_t ldb, int64_t strideB, float beta, float *C,
+                         int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream);
 
 cudaError_t launch_scale(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
                          cudaStream_t stream);
 
+// 16-bit input types of the tensor-core path.
+constexpr int kInF16 = 0;
+constexpr int kInBf16 = 1;
+
 // Returns GEMM_OK, GEMM_ERR_MISALIGNED or GEMM_ERR_LAUNCH.
-gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
-                           int64_t K, float alpha, const uint16_t *A, int64_t lda,
-                           const uint16_t *B, int64_t ldb, float beta, float *C, int64_t ldc,
+gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, int64_t M,
+                           int64_t N, int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                           int64_t strideA, const uint16_t *B, int64_t ldb, int64_t strideB,
+                           float beta, float *C, int64_t ldc, int64_t strideC, int64_t batch,
                            cudaStream_t stream);
+
+// C = beta * C for every problem of a batch (alpha == 0 or K == 0).
+cudaError_t launch_scale_batched(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
+                                 int64_t strideC, int64_t batch, cudaStream_t stream);
 
 // Reads and clears the device error word (synchronises `stream`).
 gemm_status_t read_and_clear_device_status(cudaStream_t stream);

@@ -70,6 +70,12 @@ struct HgemmParams {
     // one CTA over all of K in the same order, so the split changes no result bit.
     int64_t full_tiles, num_units;
     int tail_halves;
+    // Strided batch: batch problems share M, N, K; work units count tiles (or tile pairs)
+    // of every problem, problem b owning units [b * per_batch, (b + 1) * per_batch).
+    int64_t batch, per_batch;
+    int a_batched, b_batched;  // 0: the operand is shared by every problem (stride 0)
+    int64_t stride_c;          // elements between consecutive C matrices
+    uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
 };
 
 // Tile, column offset within it and width of work unit u.
@@ -151,25 +157,26 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag)
     atomicOr(&g_device_status, 1u);
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int32_t c0, int32_t c1)
+// Box of a 3-D tensor map (columns, rows, problem of the batch) into shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 
 // Multicast load: the box lands at the same shared-memory offset in every CTA of the cluster
 // named in cta_mask, and each of them gets the complete_tx on its barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t c0, int32_t c1, uint16_t cta_mask)
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                               int32_t c0, int32_t c1, int32_t c2, uint16_t cta_mask)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
         : "memory");
 }
 
@@ -362,8 +369,11 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 int64_t t, tm, tn;
                 int n_off, width;
                 decode_unit(p, u, t, n_off, width);
-                raster(t, rows_r, p.tiles_n, kLogGroup, tm, tn);
+                const int64_t bt = t / p.per_batch;
+                raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
                 if (MC) tm = 2 * tm + rank;
+                const int32_t ba = p.a_batched ? static_cast<int32_t>(bt) : 0;
+                const int32_t bb = p.b_batched ? static_cast<int32_t>(bt) : 0;
                 const int32_t m0 = static_cast<int32_t>(tm * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off;
                 const uint32_t bytes = A_STAGE_BYTES + uint32_t(width) * BK * 2;
@@ -383,10 +393,10 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
                         const uint32_t b_dst = sB + stage * B_STAGE_BYTES;
                         if (A_MN) {  // A stored K x M: two 64 (m) x 64 (k) boxes
-                            tma_load_2d(a_dst, &map_a, fb, m0, k0);
-                            tma_load_2d(a_dst + 8192, &map_a, fb, m0 + 64, k0);
+                            tma_load_3d(a_dst, &map_a, fb, m0, k0, ba);
+                            tma_load_3d(a_dst + 8192, &map_a, fb, m0 + 64, k0, ba);
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
-                            tma_load_2d(a_dst, &map_a, fb, k0, m0);
+                            tma_load_3d(a_dst, &map_a, fb, k0, m0, ba);
                         }
                         if (MC) {
                             // This CTA's half of the unit's B columns, multicast to both CTAs.
@@ -395,17 +405,18 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                             const uint32_t bd = b_dst + uint32_t(rank) * uint32_t(half) * 128u;
                             if (B_MN) {
                                 for (int j = 0; j < half / 64; ++j)
-                                    tma_load_2d_mc(bd + 8192 * j, &map_b, fb, nb + 64 * j, k0, kPair);
+                                    tma_load_3d_mc(bd + 8192 * j, &map_b, fb, nb + 64 * j, k0, bb, kPair);
                             } else {
-                                tma_load_2d_mc(bd, half == BN / 2 ? &map_b_half : &map_b_quarter, fb, k0, nb, kPair);
+                                tma_load_3d_mc(bd, half == BN / 2 ? &map_b_half : &map_b_quarter, fb, k0, nb, bb,
+                                               kPair);
                             }
                         } else if (B_MN) {  // B stored K x N: width / 64 boxes of 64 (n) x 64 (k)
                             for (int j = 0; j < width / 64; ++j)
-                                tma_load_2d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0);
+                                tma_load_3d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0, bb);
                         } else if (width == BN) {  // B stored N x K: one 64 (k) x 256 (n) box
-                            tma_load_2d(b_dst, &map_b, fb, k0, n0);
+                            tma_load_3d(b_dst, &map_b, fb, k0, n0, bb);
                         } else {     // half-width unit: one 64 (k) x 128 (n) box
-                            tma_load_2d(b_dst, &map_b_half, fb, k0, n0);
+                            tma_load_3d(b_dst, &map_b_half, fb, k0, n0, bb);
                         }
                     } else {
                         filled &= ~(1u << stage);  // nothing in flight on this slot
@@ -435,8 +446,9 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc_full = make_idesc(A_MN, B_MN, BN);
-            constexpr uint32_t idesc_half = make_idesc(A_MN, B_MN, BN / 2);
+            const uint32_t fmt = (p.ab_format << 7) | (p.ab_format << 10);  // A and B input type
+            const uint32_t idesc_full = make_idesc(A_MN, B_MN, BN) | fmt;
+            const uint32_t idesc_half = make_idesc(A_MN, B_MN, BN / 2) | fmt;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -500,7 +512,8 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             int64_t t, tm, tn;
             int n_off, width;
             decode_unit(p, u, t, n_off, width);
-            raster(t, rows_r, p.tiles_n, kLogGroup, tm, tn);
+            const int64_t bt = t / p.per_batch;
+            raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
             if (MC) tm = 2 * tm + rank;
             if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo)) {
                 raise_abort(abort_flag);
@@ -509,7 +522,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             tc_fence_after();
             const int64_t gm = tm * BM + row;
             const bool row_ok = gm < p.M;
-            float *crow = p.C + (row_ok ? gm * p.ldc : 0);
+            float *crow = p.C + bt * p.stride_c + (row_ok ? gm * p.ldc : 0);
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
 #pragma unroll 1
             for (int c = 0; c < width / 32; ++c) {
@@ -581,19 +594,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D fp16 tensor map over a row-major matrix of `rows` x `cols` (cols contiguous) with
-// leading dimension ld, read in boxes of box_cols x box_rows with the 128-byte swizzle.
+// 3-D tensor map over `batch` row-major matrices of `rows` x `cols` (cols contiguous) with
+// leading dimension ld, `bstride` elements apart, read in boxes of box_cols x box_rows x 1
+// with the 128-byte swizzle.  A shared operand (bstride 0) is one matrix (batch extent 1).
 bool make_map(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t cols, int64_t ld,
-              uint32_t box_cols, uint32_t box_rows)
+              uint32_t box_cols, uint32_t box_rows, int64_t batch, int64_t bstride, int bf16)
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const bool shared = bstride == 0 || batch <= 1;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(shared ? 1 : batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                                   static_cast<cuuint64_t>(shared ? ld : bstride) * 2};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<uint16_t *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -657,7 +675,8 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     }
     // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
     // half of the workers idle, its tiles are processed as two half-width units each.
-    const int64_t work = mc ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
+    p.per_batch = mc ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
+    const int64_t work = p.per_batch * p.batch;
     const int64_t workers_max = mc ? max_clusters : dev.num_sms;
     const int64_t workers = work < workers_max ? work : workers_max;
     p.full_tiles = work;
@@ -693,23 +712,27 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
 
 }  // namespace
 
-gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N, int64_t K,
-                           float alpha, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-                           float beta, float *C, int64_t ldc, cudaStream_t stream)
+gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, int64_t M, int64_t N,
+                           int64_t K, float alpha, const uint16_t *A, int64_t lda, int64_t strideA,
+                           const uint16_t *B, int64_t ldb, int64_t strideB, float beta, float *C,
+                           int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream)
 {
     if (dev.smem_optin < size_t(SMEM_BYTES)) return GEMM_ERR_NO_DEVICE;
     const int a_mn = opA == GEMM_OP_T;  // A stored K x M
     const int b_mn = opB == GEMM_OP_N;  // B stored K x N
+    const int bf = dtype == kInBf16;
     Maps m;
-    const bool ok_a = a_mn ? make_map(&m.a, A, K, M, lda, 64, BK) : make_map(&m.a, A, M, K, lda, BK, BM);
+    const bool ok_a = a_mn ? make_map(&m.a, A, K, M, lda, 64, BK, batch, strideA, bf)
+                           : make_map(&m.a, A, M, K, lda, BK, BM, batch, strideA, bf);
     bool ok_b;
     if (b_mn) {  // 64 (n) x 64 (k) boxes serve every unit width
-        ok_b = make_map(&m.b, B, K, N, ldb, 64, BK);
+        ok_b = make_map(&m.b, B, K, N, ldb, 64, BK, batch, strideB, bf);
         m.b_half = m.b;
         m.b_quarter = m.b;
     } else {     // B stored N x K: boxes of 256, 128 and 64 rows
-        ok_b = make_map(&m.b, B, N, K, ldb, BK, BN) && make_map(&m.b_half, B, N, K, ldb, BK, BN / 2) &&
-               make_map(&m.b_quarter, B, N, K, ldb, BK, BN / 4);
+        ok_b = make_map(&m.b, B, N, K, ldb, BK, BN, batch, strideB, bf) &&
+               make_map(&m.b_half, B, N, K, ldb, BK, BN / 2, batch, strideB, bf) &&
+               make_map(&m.b_quarter, B, N, K, ldb, BK, BN / 4, batch, strideB, bf);
     }
     if (!ok_a || !ok_b) return GEMM_ERR_MISALIGNED;
 
@@ -721,7 +744,12 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, i
     p.tiles_n = (N + BN - 1) / BN;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0);
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (batch <= 1 || strideC % 4 == 0);
+    p.batch = batch;
+    p.a_batched = batch > 1 && strideA != 0;
+    p.b_batched = batch > 1 && strideB != 0;
+    p.stride_c = batch > 1 ? strideC : 0;
+    p.ab_format = bf ? 1u : 0u;
     p.timeout_ns = 2000000000ull;
     p.inject_stall = 0;
     if (const char *e = std::getenv("GEMM_GB300_TEST_INJECT_STALL"); e && e[0] == '1') {

@@ -46,11 +46,12 @@ struct Plan {
 //    wave of num_sms * 3 CTAs, with at most 16 splits and at least two 16-wide slices each.
 // Split-K needs the workspace: at most kWsCounters tiles and kWsBytes of partial tiles.
 // GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps.
-Plan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_split)
+Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool allow_split)
 {
+    // a batch multiplies the tiles (and the split-K partials) of one problem
     const int KT = static_cast<int>((K + 15) / 16);
-    const int64_t tiles_l = ((M + CfgL::BM - 1) / CfgL::BM) * ((N + CfgL::BN - 1) / CfgL::BN);
-    const int64_t tiles_s = ((M + CfgS::BM - 1) / CfgS::BM) * ((N + CfgS::BN - 1) / CfgS::BN);
+    const int64_t tiles_l = ((M + CfgL::BM - 1) / CfgL::BM) * ((N + CfgL::BN - 1) / CfgL::BN) * batch;
+    const int64_t tiles_s = ((M + CfgS::BM - 1) / CfgS::BM) * ((N + CfgS::BN - 1) / CfgS::BN) * batch;
     auto fits = [&](int64_t tiles, int bm, int bn, int S) {
         return S == 1 || (allow_split && S <= KT && tiles <= int64_t(kWsCounters) &&
                           size_t(tiles) * S * bm * bn * 4 <= kWsBytes);
@@ -77,23 +78,31 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_split)
 }  // namespace
 
 cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int64_t N,
-                         int64_t K, float alpha, const float *A, int64_t lda, const float *B,
-                         int64_t ldb, float beta, float *C, int64_t ldc, cudaStream_t stream)
+                         int64_t K, float alpha, const float *A, int64_t lda, int64_t strideA,
+                         const float *B, int64_t ldb, int64_t strideB, float beta, float *C,
+                         int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream)
 {
     SgemmParams p{};
     p.M = M; p.N = N; p.K = K;
     p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.alpha = alpha; p.beta = beta;
     p.log_group = 3;
-    p.c_vec = aligned16(C) && (ldc % 4) == 0;
+    p.batch = batch;
+    p.stride_a = batch > 1 ? strideA : 0;
+    p.stride_b = batch > 1 ? strideB : 0;
+    p.stride_c = batch > 1 ? strideC : 0;
+    // 16-byte paths need every problem's base aligned: strides divisible by 4 elements
+    const bool strides4 = batch <= 1 || (strideA % 4 == 0 && strideB % 4 == 0);
+    p.c_vec = aligned16(C) && (ldc % 4) == 0 && (batch <= 1 || strideC % 4 == 0);
     // op(A) = N stores A as M x K, rows along k: staged K-major.  op(A) = T stores K x M,
     // rows along m: staged [k][m].  B likewise with n in place of m (op(B) = T is K-major).
     // 16-byte copies need a 16-byte aligned base and a leading dimension divisible by 4.
-    const bool a_vec = aligned16(A) && lda % 4 == 0, b_vec = aligned16(B) && ldb % 4 == 0;
-    Plan plan = choose_plan(M, N, K, dev.num_sms, true);
+    const bool a_vec = aligned16(A) && lda % 4 == 0 && strides4;
+    const bool b_vec = aligned16(B) && ldb % 4 == 0 && strides4;
+    Plan plan = choose_plan(M, N, K, batch, dev.num_sms, true);
     StreamWorkspace w;
     if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
-        plan = choose_plan(M, N, K, dev.num_sms, false);  // no workspace: plan without split
+        plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
     const int bm = plan.cfg == 'L' ? CfgL::BM : CfgS::BM, bn = plan.cfg == 'L' ? CfgL::BN : CfgS::BN;
     const int KT = static_cast<int>((K + 15) / 16);
     const bool transposed = plan.cfg == 'L' ? KContigModes<CfgL>::kTransposed : KContigModes<CfgS>::kTransposed;
@@ -113,6 +122,16 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     }
     return plan.cfg == 'L' ? launch_L(dev.device, a_mode, b_mode, p, stream)
                            : launch_S(dev.device, a_mode, b_mode, p, stream);
+}
+
+cudaError_t launch_scale_batched(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
+                                 int64_t strideC, int64_t batch, cudaStream_t stream)
+{
+    for (int64_t b = 0; b < batch; ++b) {
+        const cudaError_t e = launch_scale(M, N, beta, C + b * strideC, ldc, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_scale(int64_t M, int64_t N, float beta, float *C, int64_t ldc,

@@ -60,6 +60,9 @@ struct SgemmParams {
     int splits, kt_per_split;
     float *ws;               // splits x tiles partial tiles (splits > 1 only)
     unsigned int *counters;  // one arrival counter per tile, zero between launches
+    // Strided batch over gridDim.z (problems z, z + gridDim.z, ...): element offsets between
+    // consecutive problems' A, B and C (0: shared operand).
+    int64_t batch, stride_a, stride_b, stride_c;
 };
 
 template <int BM_, int BN_, int BK_, int TM_, int TN_, int STAGES_, int MIN_BLOCKS_>
@@ -338,7 +341,26 @@ __device__ __forceinline__ void load_frag_k_pair(const float *stage, int k, int 
 }
 
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
+__device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
+                                           const float *__restrict__ B, float *__restrict__ Cmat,
+                                           int64_t tile_id);
+
+template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(const SgemmParams p)
+{
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    for (int64_t z = blockIdx.z; z < p.batch; z += gridDim.z) {
+        if (z != blockIdx.z) __syncthreads();  // shared memory of the previous problem is free
+        sgemm_tile<C, A_MODE, B_MODE, SPLIT>(p, p.A + z * p.stride_a, p.B + z * p.stride_b,
+                                             p.C + z * p.stride_c, z * tiles + blockIdx.x);
+    }
+}
+
+// One output tile of one problem.  tile_id numbers the split-K partials and counters.
+template <class C, int A_MODE, int B_MODE, bool SPLIT>
+__device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
+                                           const float *__restrict__ B, float *__restrict__ Cmat,
+                                           int64_t tile_id)
 {
     extern __shared__ __align__(16) float smem[];
     float *sA = smem;
@@ -358,12 +380,12 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
     const int KT = SPLIT ? min(KT_all - kt0, p.kt_per_split) : KT_all;  // slices of this CTA
 
     const uint32_t sA_addr = smem_addr(sA), sB_addr = smem_addr(sB);
-    const SliceLoader<A_MODE, C::BM, C::BK> la(p.A, p.lda, p.M, m0, tid);
-    const SliceLoader<B_MODE, C::BN, C::BK> lb(p.B, p.ldb, p.N, n0, tid);
+    const SliceLoader<A_MODE, C::BM, C::BK> la(A, p.lda, p.M, m0, tid);
+    const SliceLoader<B_MODE, C::BN, C::BK> lb(B, p.ldb, p.N, n0, tid);
     auto load_tile = [&](int slot, int kt) {
         const int64_t k0 = int64_t(kt0 + kt) * C::BK;
-        la.load(sA_addr + slot * C::A_STAGE * 4, p.A, p.lda, k0, p.K);
-        lb.load(sB_addr + slot * C::B_STAGE * 4, p.B, p.ldb, k0, p.K);
+        la.load(sA_addr + slot * C::A_STAGE * 4, A, p.lda, k0, p.K);
+        lb.load(sB_addr + slot * C::B_STAGE * 4, B, p.ldb, k0, p.K);
     };
 
 #pragma unroll
@@ -381,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
 #pragma unroll
             for (int jb = 0; jb < C::NB; ++jb) {
                 const int64_t gn = n0 + jb * C::N_STRIDE + tx * 4;
-                if (gm < p.M && gn < p.N) prefetch_l2(p.C + gm * p.ldc + gn);
+                if (gm < p.M && gn < p.N) prefetch_l2(Cmat + gm * p.ldc + gn);
             }
         }
     }
@@ -440,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
         // order whichever CTA finishes last -- before the epilogue.
         constexpr int Q = C::TM * C::TN / 4;  // float4 per thread
         constexpr int QR = C::TN / 4;         // float4 per accumulator row
-        const int64_t tile = blockIdx.x;
+        const int64_t tile = tile_id;
         const int64_t tile4 = int64_t(C::BM) * C::BN / 4;
         float4 *all = reinterpret_cast<float4 *>(p.ws) + tile * p.splits * tile4;
 #pragma unroll
@@ -457,7 +479,9 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
             if (s_last) p.counters[tile] = 0;  // ready for the next launch
         }
         __syncthreads();
-        if (!s_last) return;
+        const bool last = s_last != 0;
+        __syncthreads();  // s_last is read before another problem of the batch reuses it
+        if (!last) return;
         __threadfence();
         // One round per split, Q independent loads in flight per round.
         for (int s2 = 0; s2 < p.splits; ++s2) {
@@ -481,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
     for (int i = 0; i < C::TM; ++i) {
         const int64_t gm = m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4);
         if (gm >= p.M) continue;
-        float *crow = p.C + gm * p.ldc;
+        float *crow = Cmat + gm * p.ldc;
 #pragma unroll
         for (int jb = 0; jb < C::NB; ++jb) {
             const int64_t gn = n0 + jb * C::N_STRIDE + tx * 4;
@@ -528,7 +552,8 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
     }
     const int64_t tiles = p.tiles_m * p.tiles_n;
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits));
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits),
+                    static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535));
     kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }

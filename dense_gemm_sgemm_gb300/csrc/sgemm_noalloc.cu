@@ -117,6 +117,7 @@ extern "C" GEMM_API gemm_status_t gemm_sgemm_f32_noalloc(gemm_op_t opA, gemm_op_
     p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.alpha = alpha; p.beta = beta;
     p.log_group = 3;
+    p.batch = 1;
     p.c_vec = aligned16(C) && (ldc % 4) == 0;
     p.tiles_m = tiles_m;
     p.tiles_n = tiles_n;

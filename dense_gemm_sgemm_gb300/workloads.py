@@ -2,9 +2,10 @@
 
 Each workload names a shape, the operand layout, alpha/beta and a value recipe.  Values
 are drawn on the CPU with ``torch.Generator().manual_seed(seed)`` in the fixed order A,
-then B, then C_in, so the same seed always gives the same bytes on any machine.  fp16
-operands are drawn in fp32 and rounded once with ``Tensor.half()`` (round to nearest
-even); consumers receive those fp16 values and never see the fp32 draw.
+then B, then C_in, so the same seed always gives the same bytes on any machine.  fp16 and
+bf16 operands are drawn in fp32 and rounded once (``Tensor.half()`` /
+``Tensor.to(torch.bfloat16)``, round to nearest even); consumers receive those 16-bit
+values and never see the fp32 draw.
 
 The shapes follow the pages this library is built from: square fp32 problems of the
 copecc "GEMM" page benchmark (section "完整优化 Kernel 源码引用"), the ragged
@@ -27,7 +28,7 @@ HGEMM_SQUARE = (2048, 4096, 8192)
 @dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str  # "f32" (SGEMM) or "f16" (fp16 inputs, fp32 accumulate and output)
+    dtype: str  # "f32" (SGEMM), "f16" or "bf16" (16-bit inputs, fp32 accumulate and output)
     M: int
     N: int
     K: int
@@ -114,6 +115,8 @@ def make_inputs(w: Workload) -> dict:
         c = torch.full((w.M, w.N), float("nan"), dtype=torch.float32)
     if w.dtype == "f16":
         a, b = a.half(), b.half()
+    elif w.dtype == "bf16":
+        a, b = a.to(torch.bfloat16), b.to(torch.bfloat16)
     return {
         "A": _padded(a, w.pad[0]),
         "B": _padded(b, w.pad[1]),

@@ -92,6 +92,51 @@ GEMM_API gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M
                                 int64_t ldc, void *stream);
 
 /*
+ * bfloat16-input GEMM with fp32 accumulation and fp32 output on the tcgen05 tensor cores:
+ * the BF16 case of the mixed-precision mode of the copecc "GEMM" page, section "Batched 执行与
+ * 混合精度" (FP16/BF16 inputs, FP32 accumulation).  Same rules as gemm_hgemm_f16f32, with
+ * A and B holding bfloat16 bit patterns (the upper halves of IEEE binary32 values).
+ */
+GEMM_API gemm_status_t gemm_bgemm_bf16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                          int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                          const uint16_t *B, int64_t ldb, float beta, float *C,
+                                          int64_t ldc, void *stream);
+
+/*
+ * Strided-batched forms (copecc "GEMM" page, section "Batched 执行与混合精度": one call runs
+ * `batch` GEMMs of the same M, N, K whose operands sit strideA, strideB and strideC elements
+ * apart).  Problem b computes
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   X_b = X + b * strideX,
+ * with the row-major rules of the single calls.  A stride of 0 shares that operand between
+ * all problems; strideC must keep the outputs apart: strideC >= (M - 1) * ldc + N when
+ * batch > 1 (else GEMM_ERR_INVALID_VALUE).  batch == 0 launches nothing.  For the 16-bit
+ * inputs the strides must also be multiples of 8 elements (else GEMM_ERR_MISALIGNED).
+ * Limits: batch <= 2^31.
+ */
+GEMM_API gemm_status_t gemm_sgemm_f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M,
+                                                      int64_t N, int64_t K, float alpha,
+                                                      const float *A, int64_t lda, int64_t strideA,
+                                                      const float *B, int64_t ldb, int64_t strideB,
+                                                      float beta, float *C, int64_t ldc,
+                                                      int64_t strideC, int64_t batch, void *stream);
+
+GEMM_API gemm_status_t gemm_hgemm_f16f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M,
+                                                         int64_t N, int64_t K, float alpha,
+                                                         const uint16_t *A, int64_t lda,
+                                                         int64_t strideA, const uint16_t *B,
+                                                         int64_t ldb, int64_t strideB, float beta,
+                                                         float *C, int64_t ldc, int64_t strideC,
+                                                         int64_t batch, void *stream);
+
+GEMM_API gemm_status_t gemm_bgemm_bf16f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M,
+                                                          int64_t N, int64_t K, float alpha,
+                                                          const uint16_t *A, int64_t lda,
+                                                          int64_t strideA, const uint16_t *B,
+                                                          int64_t ldb, int64_t strideB, float beta,
+                                                          float *C, int64_t ldc, int64_t strideC,
+                                                          int64_t batch, void *stream);
+
+/*
  * Allocation-free variant of gemm_sgemm_f32, for callers that must not allocate device
  * memory while they run: a framework whose own allocator owns the device memory and
  * forbids other cudaMalloc calls, or a latency-critical caller that cannot afford the

@@ -63,12 +63,14 @@ def _load():
         full = [ip, ip, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64, vp, i64, vp, i64, ip]
         pts = [ip, ip, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64, vp, vp, i64, vp, vp, ip]
         for name, args in (("gemm_oracle_f32", full), ("gemm_oracle_f16", full),
-                           ("gemm_oracle_f32_points", pts), ("gemm_oracle_f16_points", pts)):
+                           ("gemm_oracle_bf16", full), ("gemm_oracle_f32_points", pts),
+                           ("gemm_oracle_f16_points", pts), ("gemm_oracle_bf16_points", pts)):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
-        lib.gemm_oracle_half_to_double.argtypes = [ctypes.c_uint16]
-        lib.gemm_oracle_half_to_double.restype = ctypes.c_double
+        for dec in ("gemm_oracle_half_to_double", "gemm_oracle_bf16_to_double"):
+            getattr(lib, dec).argtypes = [ctypes.c_uint16]
+            getattr(lib, dec).restype = ctypes.c_double
         _lib = lib
         return lib
 
@@ -86,9 +88,12 @@ def _op(op) -> int:
 
 
 def _flat(x, dtype):
-    """Contiguous 1-D view of x with the given element type (fp16 passed as raw bits)."""
+    """Contiguous 1-D view of x with the given element type (fp16/bf16 passed as raw bits)."""
     a = np.asarray(x)
-    if dtype == "f16":
+    if dtype == "bf16":
+        if a.dtype != np.uint16:
+            raise TypeError("bf16 operands must be uint16 bit patterns")
+    elif dtype == "f16":
         if a.dtype == np.float16:
             a = a.view(np.uint16)
         if a.dtype != np.uint16:
@@ -128,7 +133,8 @@ def gemm(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta=0.0, Cin=None, ldcin=Non
         _check_extent("Cin", cin, M, N, ldcin)
     C = np.empty((M, N), dtype=np.float32)
     ab = np.empty((M, N), dtype=np.float64) if want_absdot else None
-    fn = _load().gemm_oracle_f16 if dtype == "f16" else _load().gemm_oracle_f32
+    fn = {"f32": _load().gemm_oracle_f32, "f16": _load().gemm_oracle_f16,
+          "bf16": _load().gemm_oracle_bf16}[dtype]
     rc = fn(opA, opB, M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
             _ptr(cin), ldcin or 0, _ptr(C), max(N, 1), _ptr(ab), max(N, 1),
             threads or default_threads())
@@ -152,8 +158,8 @@ def gemm_points(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, Cin, ldcin, rows
         cin = _flat(Cin, "f32")
     out = np.empty(rows.size, dtype=np.float32)
     ab = np.empty(rows.size, dtype=np.float64)
-    fn = (_load().gemm_oracle_f16_points if dtype == "f16"
-          else _load().gemm_oracle_f32_points)
+    fn = {"f32": _load().gemm_oracle_f32_points, "f16": _load().gemm_oracle_f16_points,
+          "bf16": _load().gemm_oracle_bf16_points}[dtype]
     rc = fn(opA, opB, M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
             _ptr(cin), ldcin or 0, _ptr(rows), _ptr(cols), rows.size, _ptr(out), _ptr(ab),
             threads or default_threads())
@@ -165,6 +171,11 @@ def gemm_points(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, Cin, ldcin, rows
 def half_to_double(bits: int) -> float:
     """The oracle's own binary16 decoder (exposed so the tests can pin it)."""
     return float(_load().gemm_oracle_half_to_double(int(bits) & 0xFFFF))
+
+
+def bf16_to_double(bits: int) -> float:
+    """The oracle's own bfloat16 decoder (exposed so the tests can pin it)."""
+    return float(_load().gemm_oracle_bf16_to_double(int(bits) & 0xFFFF))
 
 
 def tolerance_bound(ref, absdot, alpha, beta, cin, rel_tol):

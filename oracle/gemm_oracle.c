@@ -19,12 +19,14 @@
  *     opA(i,k) = A[i*lda + k]  (opA = N, A stored M x K)    or  A[k*lda + i]  (opA = T)
  *     opB(k,j) = B[k*ldb + j]  (opB = N, B stored K x N)    or  B[j*ldb + k]  (opB = T)
  *
- * Precision: every fp32 and fp16 input is converted to fp64 exactly, so each product of two
- * inputs is exact in fp64 (at most 24 + 24 significant bits).  Sums are taken in fp64 in k
+ * Precision: every fp32, fp16 and bf16 input is converted to fp64 exactly, so each product
+ * of two inputs is exact in fp64 (at most 24 + 24 significant bits).  Sums are taken in fp64 in k
  * order.  beta == 0 means Cin is not read at all (BLAS convention), so NaN or Inf in Cin does
  * not reach the result.  The fp16 inputs are decoded from their bit patterns by the decoder
  * below, written from the IEEE 754 binary16 definition (1 sign bit, 5 exponent bits with bias
- * 15, 10 fraction bits; exponent 0 = zero/subnormal, exponent 31 = Inf/NaN).
+ * 15, 10 fraction bits; exponent 0 = zero/subnormal, exponent 31 = Inf/NaN); bf16 inputs
+ * (mixed precision with BF16 inputs, copecc "GEMM" page, section "Batched 执行与混合精度") are
+ * the upper 16 bits of an IEEE binary32 pattern.
  *
  * Optionally the oracle also returns absdot[i][j] = sum_k |opA(i,k) * opB(k,j)|, the
  * quantity the acceptance bound of the parity tests is written in.
@@ -58,8 +60,18 @@ double gemm_oracle_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* bfloat16 -> double, exact: the 16 bits are the upper half of an IEEE binary32 pattern
+ * (1 sign bit, 8 exponent bits with bias 127, 7 fraction bits). */
+double gemm_oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
 typedef struct {
-    int dtype; /* 0 = fp32 inputs, 1 = fp16 inputs */
+    int dtype; /* 0 = fp32 inputs, 1 = fp16 inputs, 2 = bf16 inputs */
     int opA, opB;
     int64_t M, N, K;
     double alpha, beta;
@@ -85,6 +97,7 @@ typedef struct {
 static inline double load_in(const job_t *j, const void *base, int64_t idx)
 {
     if (j->dtype == 0) return (double)((const float *)base)[idx];
+    if (j->dtype == 2) return gemm_oracle_bf16_to_double(((const uint16_t *)base)[idx]);
     return gemm_oracle_half_to_double(((const uint16_t *)base)[idx]);
 }
 
@@ -135,7 +148,8 @@ static void rows_opBN(const job_t *j, double *acc, double *aacc)
             } else {
                 const uint16_t *brow = (const uint16_t *)j->B + k * j->ldb;
                 for (int64_t c = 0; c < j->N; ++c) {
-                    double p = a * gemm_oracle_half_to_double(brow[c]);
+                    double p = a * (j->dtype == 2 ? gemm_oracle_bf16_to_double(brow[c])
+                                                  : gemm_oracle_half_to_double(brow[c]));
                     acc[c] += p;
                     aacc[c] += fabs(p);
                 }
@@ -259,6 +273,25 @@ int gemm_oracle_f16(int opA, int opB, int64_t M, int64_t N, int64_t K, double al
 {
     return full(1, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, Cin, ldcin, Cout, ldc,
                 absdot, ldabs, nthreads);
+}
+
+int gemm_oracle_bf16(int opA, int opB, int64_t M, int64_t N, int64_t K, double alpha,
+                     const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, double beta,
+                     const float *Cin, int64_t ldcin, float *Cout, int64_t ldc, double *absdot,
+                     int64_t ldabs, int nthreads)
+{
+    return full(2, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, Cin, ldcin, Cout, ldc,
+                absdot, ldabs, nthreads);
+}
+
+int gemm_oracle_bf16_points(int opA, int opB, int64_t M, int64_t N, int64_t K, double alpha,
+                            const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                            double beta, const float *Cin, int64_t ldcin, const int64_t *rows,
+                            const int64_t *cols, int64_t npts, float *out, double *abs_out,
+                            int nthreads)
+{
+    return points(2, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, Cin, ldcin, rows, cols,
+                  npts, out, abs_out, nthreads);
 }
 
 int gemm_oracle_f32_points(int opA, int opB, int64_t M, int64_t N, int64_t K, double alpha,

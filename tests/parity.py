@@ -2,8 +2,10 @@
 
 Acceptance (per element, from the definition of the method and the stated tolerances):
     |C - C_ref| <= tol * (|alpha| * sum_k |a_ik b_kj| + |beta| * |Cin_ij|) + ulp32(|C_ref|)
-with tol = 1e-5 for strict FP32 and 2e-3 for fp16 inputs with fp32 accumulation, and bit
-equality when every input is a small integer (all partial sums are then exact in fp32).
+with tol = 1e-5 for strict FP32 and 2e-3 for fp16 (and bf16) inputs with fp32
+accumulation, and bit equality when every input is a small integer (all partial sums are
+then exact in fp32).  The 16-bit inputs are the rounded values both sides consume, so the
+tolerance covers only the fp32 accumulation, whose error does not depend on the input type.
 """
 from __future__ import annotations
 
@@ -11,9 +13,9 @@ import numpy as np
 import torch
 
 import oracle
-from dense_gemm_sgemm_gb300 import gemm_hgemm_f16f32, gemm_sgemm_f32, workloads
+from dense_gemm_sgemm_gb300 import gemm_bgemm_bf16f32, gemm_hgemm_f16f32, gemm_sgemm_f32, workloads
 
-TOL = {"f32": 1e-5, "f16": 2e-3}
+TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
 
 
 def to_device(inputs: dict) -> dict:
@@ -21,14 +23,21 @@ def to_device(inputs: dict) -> dict:
 
 
 def run_library(w: workloads.Workload, dev: dict, stream=None):
-    fn = gemm_sgemm_f32 if w.dtype == "f32" else gemm_hgemm_f16f32
+    fn = {"f32": gemm_sgemm_f32, "f16": gemm_hgemm_f16f32, "bf16": gemm_bgemm_bf16f32}[w.dtype]
     fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, dev["A"], w.lda, dev["B"], w.ldb, w.beta,
        dev["C"], w.ldc, stream)
 
 
-def _np_in(t: torch.Tensor, dtype: str):
-    a = t.contiguous().cpu().numpy()
+def np_in(t: torch.Tensor, dtype: str):
+    """numpy view of an operand: fp32 values, or the raw bits of fp16 / bf16 values."""
+    t = t.contiguous().cpu()
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16)
+    a = t.numpy()
     return a.view(np.uint16) if dtype == "f16" else a
+
+
+_np_in = np_in
 
 
 def oracle_full(w: workloads.Workload, inputs: dict):

@@ -22,6 +22,14 @@ pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
 
 # ----------------------------------------------------------------------------- helpers
+def _bf16_bits(values64):
+    """bfloat16 bit patterns of float64 values (rounded by torch, round to nearest even)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(values64, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 def _store(logical, op, pad, dtype):
     """Stored buffer (flat) and ld of a logical matrix for the given op and row padding."""
     mat = np.asarray(logical, dtype=np.float64)
@@ -30,6 +38,8 @@ def _store(logical, op, pad, dtype):
     ld = cols + pad
     buf = np.full((rows, ld), np.nan, dtype=np.float64)
     buf[:, :cols] = stored
+    if dtype == "bf16":
+        return _bf16_bits(buf).reshape(-1), ld
     np_t = np.float32 if dtype == "f32" else np.float16
     return buf.astype(np_t).reshape(-1), ld
 
@@ -65,7 +75,7 @@ def _same(a, b):
 
 
 # ------------------------------------------------------- brute force on tiny shapes
-@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_brute_force_exact_rationals(dtype):
     rng = np.random.default_rng(1234)
     cases = 0
@@ -92,6 +102,17 @@ def test_half_decoder_matches_numpy_on_every_bit_pattern():
     want = bits.view(np.float16).astype(np.float64)
     lib = oracle._load()
     got = np.array([lib.gemm_oracle_half_to_double(int(b)) for b in bits])
+    both_nan = np.isnan(want) & np.isnan(got)
+    assert np.all(both_nan | (got == want))
+    assert np.array_equal(np.signbit(got[~both_nan]), np.signbit(want[~both_nan]))
+
+
+def test_bf16_decoder_matches_torch_on_every_bit_pattern():
+    import torch
+
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
     both_nan = np.isnan(want) & np.isnan(got)
     assert np.all(both_nan | (got == want))
     assert np.array_equal(np.signbit(got[~both_nan]), np.signbit(want[~both_nan]))
@@ -249,6 +270,7 @@ _MUTANTS = {
     "beta_sign_flipped": ("if (j->beta != 0.0) r += j->beta", "if (j->beta != 0.0) r -= j->beta"),
     "half_exponent_bias_off_by_one": ("expo - 25", "expo - 24"),
     "alpha_ignored_in_row_kernel": ("double r = j->alpha * acc[c];", "double r = acc[c];"),
+    "bf16_bits_misplaced": ("uint32_t bits = (uint32_t)h << 16;", "uint32_t bits = (uint32_t)h << 15;"),
 }
 
 
@@ -270,14 +292,15 @@ def _pins_pass_with(lib):
     try:
         i64, dbl, ip, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p
         full = [ip, ip, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64, vp, i64, vp, i64, ip]
-        for nm in ("gemm_oracle_f32", "gemm_oracle_f16"):
+        for nm in ("gemm_oracle_f32", "gemm_oracle_f16", "gemm_oracle_bf16"):
             getattr(lib, nm).argtypes = full
             getattr(lib, nm).restype = ctypes.c_int
-        lib.gemm_oracle_half_to_double.argtypes = [ctypes.c_uint16]
-        lib.gemm_oracle_half_to_double.restype = ctypes.c_double
+        for dec in ("gemm_oracle_half_to_double", "gemm_oracle_bf16_to_double"):
+            getattr(lib, dec).argtypes = [ctypes.c_uint16]
+            getattr(lib, dec).restype = ctypes.c_double
         oracle._lib = lib
         rng = np.random.default_rng(2024)
-        for dtype in ("f32", "f16"):
+        for dtype in ("f32", "f16", "bf16"):
             for (M, N, K), opA, opB in itertools.product([(3, 4, 3), (5, 2, 2), (2, 3, 1)],
                                                          "NT", "NT"):
                 Alog = _values(rng, (M, K), "dyadic")
