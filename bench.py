@@ -142,12 +142,22 @@ def whole_job_value(local_total_ms, steps, flops_per_step, world, device=None):
     return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12, total_ms
 
 
-def _traffic_from_profile(kernel_file: str, profile: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches today's source."""
+def csrc_digest() -> str:
+    """First 16 hex digits of a sha256 over every CUDA source of the library."""
+    import glob
+
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "dense_gemm_sgemm_gb300", "csrc", "*"))):
+        h.update(os.path.basename(path).encode())
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(profile: str):
+    """DRAM bytes per launch from a committed ncu summary, if the sources are unchanged."""
     path = os.path.join(ROOT, "profiles", profile)
-    src = os.path.join(ROOT, "dense_gemm_sgemm_gb300", "csrc", kernel_file)
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = csrc_digest()
         fields = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
@@ -335,13 +345,13 @@ def run_ours(args, rank, world, local):
     mean_ms = statistics.fmean(step_ms)
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
     if w.dtype == "f32":
-        kernel_src, kernel = "sgemm_ffma.cu", "sgemm_ffma"
+        kernel = "sgemm_ffma"
         bound, peak, peak_src = "alu", FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
     else:
-        kernel_src, kernel = "hgemm_tcgen05.cu", "hgemm_tcgen05"
+        kernel = "hgemm_tcgen05"
         bound, peak = "tensor", peaks["bf16_tflops"]
         peak_src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
-    traffic = _traffic_from_profile(kernel_src, f"{kernel}_{w.name}.txt")
+    traffic = _traffic_from_profile(f"{kernel}_{w.name}.txt")
     vs = (round(value / (PAGES_RAGGED_GFLOPS / 1e3), 4)
           if w.name == workloads.sgemm_ragged().name else None)
     line = {
