@@ -532,31 +532,35 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 const int64_t gn0 = tn * BN + n_off + c * 32;
                 if (!row_ok || gn0 >= p.N) continue;
                 if (p.c_vec && gn0 + 32 <= p.N) {
+                    float4 *dst = reinterpret_cast<float4 *>(crow + gn0);
+                    if (beta != 0.0f) {  // all eight reads of C in flight before any store
+                        float4 ci[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float4 o;
-                        float4 *dst = reinterpret_cast<float4 *>(crow + gn0 + 4 * j);
-                        if (beta != 0.0f) {
-                            const float4 ci = *dst;
-                            o.x = fmaf(alpha, v[4 * j + 0], beta * ci.x);
-                            o.y = fmaf(alpha, v[4 * j + 1], beta * ci.y);
-                            o.z = fmaf(alpha, v[4 * j + 2], beta * ci.z);
-                            o.w = fmaf(alpha, v[4 * j + 3], beta * ci.w);
-                        } else {
-                            o = make_float4(alpha * v[4 * j], alpha * v[4 * j + 1], alpha * v[4 * j + 2],
-                                            alpha * v[4 * j + 3]);
-                        }
-                        *dst = o;
+                        for (int j = 0; j < 8; ++j) ci[j] = dst[j];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(fmaf(alpha, v[4 * j + 0], beta * ci[j].x),
+                                                 fmaf(alpha, v[4 * j + 1], beta * ci[j].y),
+                                                 fmaf(alpha, v[4 * j + 2], beta * ci[j].z),
+                                                 fmaf(alpha, v[4 * j + 3], beta * ci[j].w));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(alpha * v[4 * j], alpha * v[4 * j + 1], alpha * v[4 * j + 2],
+                                                 alpha * v[4 * j + 3]);
                     }
                 } else {
+                    if (beta != 0.0f) {  // reads first, then stores
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int64_t gn = gn0 + j;
-                        if (gn < p.N) {
-                            float *dst = crow + gn;
-                            *dst = beta != 0.0f ? fmaf(alpha, v[j], beta * *dst) : alpha * v[j];
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = fmaf(alpha, v[j], gn0 + j < p.N ? beta * crow[gn0 + j] : 0.0f);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= alpha;
                     }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (gn0 + j < p.N) crow[gn0 + j] = v[j];
                 }
             }
             tc_fence_before();

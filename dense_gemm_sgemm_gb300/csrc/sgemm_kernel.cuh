@@ -501,37 +501,93 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 
     // Epilogue: C = alpha * acc + beta * C, beta == 0 never reads C.
     const float alpha = p.alpha, beta = p.beta;
+    auto row_of = [&](int i) { return m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4); };
+    auto col_of = [&](int jb) { return n0 + jb * C::N_STRIDE + tx * 4; };
+    if constexpr (C::TM * C::TN > 16) {
+        // Large thread tiles (long-running CTAs): one pass, read-modify-write per 4-vector.
+#pragma unroll
+        for (int i = 0; i < C::TM; ++i) {
+            const int64_t gm = row_of(i);
+            if (gm >= p.M) continue;
+            float *crow = Cmat + gm * p.ldc;
+#pragma unroll
+            for (int jb = 0; jb < C::NB; ++jb) {
+                const int64_t gn = col_of(jb);
+                const float2 lo = acc[i][2 * jb], hi = acc[i][2 * jb + 1];
+                float v[4] = {lo.x, lo.y, hi.x, hi.y};
+                if (p.c_vec && gn + 3 < p.N) {
+                    float4 o;
+                    if (beta != 0.0f) {
+                        const float4 cin = *reinterpret_cast<const float4 *>(crow + gn);
+                        o = make_float4(fmaf(alpha, v[0], beta * cin.x), fmaf(alpha, v[1], beta * cin.y),
+                                        fmaf(alpha, v[2], beta * cin.z), fmaf(alpha, v[3], beta * cin.w));
+                    } else {
+                        o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                    }
+                    *reinterpret_cast<float4 *>(crow + gn) = o;
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (gn + jj < p.N)
+                            crow[gn + jj] = beta != 0.0f ? fmaf(alpha, v[jj], beta * crow[gn + jj]) : alpha * v[jj];
+                }
+            }
+        }
+        return;
+    }
+    // Small thread tiles (short-lived CTAs, where the epilogue is a large share of the time):
+    // two passes, first every read of C (loads only, so they are all in flight together),
+    // then every store.
+    if (beta != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < C::TM; ++i) {
+            const int64_t gm = row_of(i);
+            if (gm >= p.M) continue;
+            const float *crow = Cmat + gm * p.ldc;
+#pragma unroll
+            for (int jb = 0; jb < C::NB; ++jb) {
+                const int64_t gn = col_of(jb);
+                float2 &lo = acc[i][2 * jb], &hi = acc[i][2 * jb + 1];
+                float4 cin;
+                if (p.c_vec && gn + 3 < p.N) {
+                    cin = *reinterpret_cast<const float4 *>(crow + gn);
+                } else {
+                    cin.x = gn + 0 < p.N ? crow[gn + 0] : 0.0f;
+                    cin.y = gn + 1 < p.N ? crow[gn + 1] : 0.0f;
+                    cin.z = gn + 2 < p.N ? crow[gn + 2] : 0.0f;
+                    cin.w = gn + 3 < p.N ? crow[gn + 3] : 0.0f;
+                }
+                lo.x = fmaf(alpha, lo.x, beta * cin.x);
+                lo.y = fmaf(alpha, lo.y, beta * cin.y);
+                hi.x = fmaf(alpha, hi.x, beta * cin.z);
+                hi.y = fmaf(alpha, hi.y, beta * cin.w);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < C::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < C::TN / 2; ++j) {
+                acc[i][j].x *= alpha;
+                acc[i][j].y *= alpha;
+            }
+    }
 #pragma unroll
     for (int i = 0; i < C::TM; ++i) {
-        const int64_t gm = m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4);
+        const int64_t gm = row_of(i);
         if (gm >= p.M) continue;
         float *crow = Cmat + gm * p.ldc;
 #pragma unroll
         for (int jb = 0; jb < C::NB; ++jb) {
-            const int64_t gn = n0 + jb * C::N_STRIDE + tx * 4;
+            const int64_t gn = col_of(jb);
             const float2 lo = acc[i][2 * jb], hi = acc[i][2 * jb + 1];
-            float v[4] = {lo.x, lo.y, hi.x, hi.y};
             if (p.c_vec && gn + 3 < p.N) {
-                float4 o;
-                if (beta != 0.0f) {
-                    const float4 cin = *reinterpret_cast<const float4 *>(crow + gn);
-                    o.x = fmaf(alpha, v[0], beta * cin.x);
-                    o.y = fmaf(alpha, v[1], beta * cin.y);
-                    o.z = fmaf(alpha, v[2], beta * cin.z);
-                    o.w = fmaf(alpha, v[3], beta * cin.w);
-                } else {
-                    o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
-                }
-                *reinterpret_cast<float4 *>(crow + gn) = o;
+                *reinterpret_cast<float4 *>(crow + gn) = make_float4(lo.x, lo.y, hi.x, hi.y);
             } else {
+                const float v[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    if (gn + jj < p.N) {
-                        const float r = beta != 0.0f ? fmaf(alpha, v[jj], beta * crow[gn + jj])
-                                                     : alpha * v[jj];
-                        crow[gn + jj] = r;
-                    }
-                }
+                for (int jj = 0; jj < 4; ++jj)
+                    if (gn + jj < p.N) crow[gn + jj] = v[jj];
             }
         }
     }
