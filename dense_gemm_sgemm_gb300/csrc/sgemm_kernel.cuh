@@ -60,8 +60,8 @@ struct SgemmParams {
     int splits, kt_per_split;
     float *ws;               // splits x tiles partial tiles (splits > 1 only)
     unsigned int *counters;  // one arrival counter per tile, zero between launches
-    // Strided batch over gridDim.z (problems z, z + gridDim.z, ...): element offsets between
-    // consecutive problems' A, B and C (0: shared operand).
+    // Strided batch: problem blockIdx.z of a launch (batch problems in all); element offsets
+    // between consecutive problems' A, B and C (0: shared operand).
     int64_t batch, stride_a, stride_b, stride_c;
 };
 
@@ -348,12 +348,11 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(const SgemmParams p)
 {
-    const int64_t tiles = p.tiles_m * p.tiles_n;
-    for (int64_t z = blockIdx.z; z < p.batch; z += gridDim.z) {
-        if (z != blockIdx.z) __syncthreads();  // shared memory of the previous problem is free
-        sgemm_tile<C, A_MODE, B_MODE, SPLIT>(p, p.A + z * p.stride_a, p.B + z * p.stride_b,
-                                             p.C + z * p.stride_c, z * tiles + blockIdx.x);
-    }
+    // One problem per CTA: problem blockIdx.z of this launch (the host launches batches of
+    // more than 65535 problems in chunks).
+    const int64_t z = blockIdx.z;
+    sgemm_tile<C, A_MODE, B_MODE, SPLIT>(p, p.A + z * p.stride_a, p.B + z * p.stride_b, p.C + z * p.stride_c,
+                                         z * (p.tiles_m * p.tiles_n) + blockIdx.x);
 }
 
 // One output tile of one problem.  tile_id numbers the split-K partials and counters.
@@ -382,10 +381,12 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     const uint32_t sA_addr = smem_addr(sA), sB_addr = smem_addr(sB);
     const SliceLoader<A_MODE, C::BM, C::BK> la(A, p.lda, p.M, m0, tid);
     const SliceLoader<B_MODE, C::BN, C::BK> lb(B, p.ldb, p.N, n0, tid);
+    // Copies that read nothing (zero fill) still need a valid address: the parameter-space
+    // bases, which cost no registers.
     auto load_tile = [&](int slot, int kt) {
         const int64_t k0 = int64_t(kt0 + kt) * C::BK;
-        la.load(sA_addr + slot * C::A_STAGE * 4, A, p.lda, k0, p.K);
-        lb.load(sB_addr + slot * C::B_STAGE * 4, B, p.ldb, k0, p.K);
+        la.load(sA_addr + slot * C::A_STAGE * 4, p.A, p.lda, k0, p.K);
+        lb.load(sB_addr + slot * C::B_STAGE * 4, p.B, p.ldb, k0, p.K);
     };
 
 #pragma unroll
@@ -423,6 +424,23 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 
         const float *As = sA + (kt % C::STAGES) * C::A_STAGE;
         const float *Bs = sB + (kt % C::STAGES) * C::B_STAGE;
+        if constexpr (!is_k_major(A_MODE) && !is_k_major(B_MODE)) {
+            // both operands [k][x]: one k at a time, 128-bit fragment reads
+#pragma unroll
+            for (int k = 0; k < C::BK; ++k) {
+                float a[C::TM], b[C::TN];
+                load_frag_mn<C::BM, C::TM, C::M_STRIDE>(As, k, ty, a);
+                load_frag_mn<C::BN, C::TN, C::N_STRIDE>(Bs, k, tx, b);
+#pragma unroll
+                for (int i = 0; i < C::TM; ++i) {
+                    const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < C::TN / 2; ++j)
+                        acc[i][j] = __ffma2_rn(ai, make_float2(b[2 * j], b[2 * j + 1]), acc[i][j]);
+                }
+            }
+            continue;
+        }
 #pragma unroll
         for (int k = 0; k < C::BK; k += 2) {
             // K-major operands come in k pairs; [k][m] / [k][n] operands one k at a time.
@@ -608,10 +626,21 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
     }
     const int64_t tiles = p.tiles_m * p.tiles_n;
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits),
-                    static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535));
-    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    // gridDim.z holds at most 65535 problems: larger batches go in consecutive launches on the
+    // same stream (which also keeps their split-K workspace use in order).
+    constexpr int64_t kMaxZ = 65535;
+    for (int64_t b0 = 0; b0 < p.batch; b0 += kMaxZ) {
+        SgemmParams q = p;
+        q.batch = p.batch - b0 < kMaxZ ? p.batch - b0 : kMaxZ;
+        q.A = p.A + b0 * p.stride_a;
+        q.B = p.B + b0 * p.stride_b;
+        q.C = p.C + b0 * p.stride_c;
+        const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits), static_cast<unsigned>(q.batch));
+        kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(q);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Staging of K-contiguous operands per tile configuration: the 8 x 8 thread tile keeps the
