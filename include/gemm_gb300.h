@@ -81,10 +81,14 @@ GEMM_API gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, i
  * (the mixed-precision mode of the copecc "GEMM" page, section "Batched 执行与混合精度", and
  * of the dandandamowang.xyz "GEMM优化（二）" page): products of IEEE binary16 inputs are
  * summed in fp32, then C = alpha * sum + beta * C in fp32.
- * A, B: IEEE binary16 bit patterns (uint16_t), base 16-byte aligned, and lda, ldb
- * multiples of 8 elements (the tensor-memory-access unit moves 16-byte granules);
- * otherwise GEMM_ERR_MISALIGNED.  C: fp32, 4-byte aligned, any ldc.
- * Limits: M, N, K < 2^31; lda, ldb < 2^36 bytes.
+ * A, B: IEEE binary16 bit patterns (uint16_t), 2-byte aligned, any lda, ldb.  The
+ * tensor-memory-access unit reads 16-byte granules, so an operand whose base is not 16-byte
+ * aligned or whose lda (ldb) is not a multiple of 8 elements is first copied into a scratch
+ * buffer of this stream with the leading dimension rounded up (the buffer is allocated on
+ * first need, grows when a larger operand needs it, and is kept until exit; during stream
+ * capture no buffer can be allocated and such an operand gives GEMM_ERR_MISALIGNED).
+ * C: fp32, 4-byte aligned, any ldc.
+ * Limits: M, N, K < 2^31; lda, ldb < 2^35 elements.
  */
 GEMM_API gemm_status_t gemm_hgemm_f16f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
                                 int64_t K, float alpha, const uint16_t *A, int64_t lda,
@@ -109,8 +113,9 @@ GEMM_API gemm_status_t gemm_bgemm_bf16f32(gemm_op_t opA, gemm_op_t opB, int64_t 
  *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   X_b = X + b * strideX,
  * with the row-major rules of the single calls.  A stride of 0 shares that operand between
  * all problems; strideC must keep the outputs apart: strideC >= (M - 1) * ldc + N when
- * batch > 1 (else GEMM_ERR_INVALID_VALUE).  batch == 0 launches nothing.  For the 16-bit
- * inputs the strides must also be multiples of 8 elements (else GEMM_ERR_MISALIGNED).
+ * batch > 1 (else GEMM_ERR_INVALID_VALUE).  batch == 0 launches nothing.  A 16-bit
+ * operand whose batch stride is not a multiple of 8 elements is packed like an unaligned
+ * leading dimension (see gemm_hgemm_f16f32).
  * Limits: batch <= 2^31.
  */
 GEMM_API gemm_status_t gemm_sgemm_f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M,

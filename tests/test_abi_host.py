@@ -85,9 +85,9 @@ def test_argument_validation_needs_no_device(lib):
     assert f(0, 0, 0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, None) == 0  # empty: no launch
     assert f(0, 0, 1 << 31, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 3
     assert f(0, 0, 4, 4, 4, 1.0, P + 2, 4, P, 4, 0.0, P, 4, None) == 2  # A not 4-byte aligned
-    assert h(0, 0, 4, 4, 8, 1.0, P + 8, 8, P, 8, 0.0, P, 4, None) == 2  # A not 16-byte aligned
-    assert h(0, 0, 4, 8, 4, 1.0, P, 4, P, 8, 0.0, P, 8, None) == 2      # lda not a multiple of 8
-    assert h(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 2
+    assert h(0, 0, 4, 4, 8, 1.0, P + 1, 8, P, 8, 0.0, P, 4, None) == 2  # A not 2-byte aligned
+    assert h(0, 0, 4, 4, 8, 1.0, P, 8, P + 3, 8, 0.0, P, 4, None) == 2  # B not 2-byte aligned
+    assert h(0, 0, 4, 4, 8, 1.0, P, 8, P, 8, 0.0, P + 2, 4, None) == 2  # C not 4-byte aligned
     # K == 0 or alpha == 0 does not need A or B
     assert f(0, 0, 0, 0, 0, 0.0, None, 1, None, 1, 0.0, None, 1, None) == 0
 

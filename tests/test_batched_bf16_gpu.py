@@ -126,6 +126,17 @@ def test_tensor_core_strided_batched(dtype, opA, opB):
     _check_batched(_batched_case(dtype, 3, 300, 520, 192, opA, opB, seed=4))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tensor_core_strided_batched_unaligned_strides_are_packed(dtype):
+    c = _batched_case(dtype, 3, 200, 136, 100, "N", "T", seed=6)
+    # shift every problem's operands by an odd number of elements
+    c["sA"] += 3
+    c["sB"] += 1
+    c["A"] = torch.cat([c["A"], torch.zeros(3 * 3, dtype=c["A"].dtype)])
+    c["B"] = torch.cat([c["B"], torch.zeros(3, dtype=c["B"].dtype)])
+    _check_batched(c)
+
+
 def test_tensor_core_strided_batched_shared_b():
     _check_batched(_batched_case("f16", 4, 256, 256, 128, "N", "T", share_b=True, seed=5))
 
@@ -141,9 +152,9 @@ def test_batched_argument_rules():
         g.gemm_sgemm_f32_strided_batched("N", "N", 8, 8, 8, 1.0, A, 8, 64, A, 8, 64, 0.0, A, 8,
                                          64, -1)
     assert e.value.status == 1
-    with pytest.raises(GemmError) as e:  # 16-bit strides must be multiples of 8 elements
-        g.gemm_hgemm_f16f32_strided_batched("N", "N", 8, 8, 8, 1.0, H, 8, 68, H, 8, 64, 0.0, A,
-                                            8, 64, 2)
+    with pytest.raises(GemmError) as e:  # odd byte address
+        g.gemm_hgemm_f16f32_strided_batched("N", "N", 8, 8, 8, 1.0, H.data_ptr() + 1, 8, 64, H, 8,
+                                            64, 0.0, A, 8, 64, 2)
     assert e.value.status == 2
     # batch == 0 is a no-op
     g.gemm_sgemm_f32_strided_batched("N", "N", 8, 8, 8, 1.0, A, 8, 64, A, 8, 64, 0.0, A, 8, 64, 0)
