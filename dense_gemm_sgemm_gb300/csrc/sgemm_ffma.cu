@@ -33,43 +33,94 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr size_t kWsBytes = kWorkspaceBytes;
 constexpr size_t kWsCounters = kWorkspaceCounters;
 
-// A launch plan: tile configuration ('L' = 128 x 128, 'S' = 64 x 64) and K splits.
+// One tile configuration as the host sees it, with its cost-model constants (microseconds,
+// fitted by least squares on log time to 1,600 timed launches on GB300: ten M x N shapes from
+// 256^2 to 3072^2, K = 128 / 513 / 1024 / 4096, op(A) = N and T, every configuration and split
+// count below; the rule picks a plan within 1.6% of the fastest measured one on average).
+struct CfgDesc {
+    char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
+    int bm, bn, min_blocks;
+    bool transposed;  // K-contiguous operands staged [k][x] (kKT)
+    int max_splits;
+    double us_slice;   // one K slice of one CTA, per co-resident CTA of the same SM
+    double us_fixed;   // per wave of CTAs: prologue, epilogue, launch ramp
+    double us_split;   // per split: partial-tile traffic and the fixed-order sum
+    cudaError_t (*launch)(int, int, int, const SgemmParams &, cudaStream_t);
+    cudaError_t (*launch_split)(int, int, int, const SgemmParams &, cudaStream_t);
+};
+
+using Launcher = cudaError_t (*)(int, int, int, const SgemmParams &, cudaStream_t);
+
+template <class C>
+constexpr CfgDesc desc(char name, int max_splits, double us_slice, double us_fixed, double us_split,
+                       Launcher l, Launcher ls)
+{
+    return CfgDesc{name, C::BM, C::BN, C::MIN_BLOCKS, KContigModes<C>::kTransposed, max_splits,
+                   us_slice, us_fixed, us_split, l, ls};
+}
+
+const CfgDesc kCfgs[] = {
+    desc<CfgL>('L', 4, 1.442, 3.156, 1.764, launch_L, launch_LS),
+    desc<CfgM>('M', 12, 0.857, 1.723, 0.464, launch_M, launch_MS),
+    desc<CfgS>('S', 16, 0.471, 1.429, 0.015, launch_S, launch_SS),
+};
+
+const CfgDesc *find_cfg(char name)
+{
+    for (const CfgDesc &c : kCfgs)
+        if (c.name == name) return &c;
+    return nullptr;
+}
+
+// A launch plan: tile configuration and K splits.
 struct Plan {
-    char cfg;
+    const CfgDesc *cfg;
     int splits;
 };
 
-// Plan rule, fitted to measurements on GB300 (fp32, flushed L2):
-//  * when the 128 x 128 tiles alone give every SM a tile, use them unsplit (best per-flop
-//    throughput: 8 x 8 outer products, 128-bit fragment reads);
-//  * otherwise use 64 x 64 tiles (three CTAs per SM) and split K so that the grid fills one
-//    wave of num_sms * 3 CTAs, with at most 16 splits and at least two 16-wide slices each.
+// Plan rule: the (configuration, splits) pair of least modelled time.  CTAs run in waves of
+// num_sms * min_blocks; the CTAs that share an SM share its FMA pipes, so a wave lasts
+// (slices per CTA) * (CTAs on the busiest SM) * us_slice + us_fixed, and every split adds
+// us_split.  Splits come from {1, 2, 3, 4, 6, 8, 12, 16} (at most max_splits, at least two
+// K slices each) and cost 2% extra in the comparison, so near ties keep K whole.
 // Split-K needs the workspace: at most kWsCounters tiles and kWsBytes of partial tiles.
 // GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps.
 Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool allow_split)
 {
     // a batch multiplies the tiles (and the split-K partials) of one problem
-    const int KT = static_cast<int>((K + 15) / 16);
-    const int64_t tiles_l = ((M + CfgL::BM - 1) / CfgL::BM) * ((N + CfgL::BN - 1) / CfgL::BN) * batch;
-    const int64_t tiles_s = ((M + CfgS::BM - 1) / CfgS::BM) * ((N + CfgS::BN - 1) / CfgS::BN) * batch;
-    auto fits = [&](int64_t tiles, int bm, int bn, int S) {
-        return S == 1 || (allow_split && S <= KT && tiles <= int64_t(kWsCounters) &&
-                          size_t(tiles) * S * bm * bn * 4 <= kWsBytes);
+    const int64_t KT = (K + 15) / 16;
+    auto tiles = [&](const CfgDesc &c) { return ((M + c.bm - 1) / c.bm) * ((N + c.bn - 1) / c.bn) * batch; };
+    auto fits = [&](const CfgDesc &c, int S) {
+        return S == 1 || (allow_split && S <= KT && S <= c.max_splits && tiles(c) <= int64_t(kWsCounters) &&
+                          size_t(tiles(c)) * S * c.bm * c.bn * 4 <= kWsBytes);
     };
-    Plan plan{'L', 1};
-    if (tiles_l < num_sms) {
-        const int64_t target = int64_t(num_sms) * CfgS::MIN_BLOCKS;
-        int S = static_cast<int>((target + tiles_s / 2) / tiles_s);
-        S = S < 1 ? 1 : (S > 16 ? 16 : S);
-        while (S > 1 && (KT / S < 2 || !fits(tiles_s, CfgS::BM, CfgS::BN, S))) --S;
-        plan = {'S', S};
-    }
+    auto cost = [&](const CfgDesc &c, int S) {
+        const int64_t ctas = tiles(c) * S;
+        const double kps = double((KT + S - 1) / S);
+        const int64_t slots = int64_t(num_sms) * c.min_blocks;
+        const int64_t full = ctas / slots, rem = ctas % slots;
+        double t = double(full) * (kps * c.min_blocks * c.us_slice + c.us_fixed);
+        if (rem > 0) t += kps * double((rem + num_sms - 1) / num_sms) * c.us_slice + c.us_fixed;
+        if (S > 1) t = (t + S * c.us_split) * 1.02;
+        return t;
+    };
+    static const int kSplits[] = {1, 2, 3, 4, 6, 8, 12, 16};
+    Plan plan{find_cfg('L'), 1};
+    double best = -1.0;
+    for (const CfgDesc &c : kCfgs)
+        for (int S : kSplits) {
+            if (!fits(c, S) || (S > 1 && KT / S < 2)) continue;
+            const double t = cost(c, S);
+            if (best < 0.0 || t < best) {
+                best = t;
+                plan = {&c, S};
+            }
+        }
     if (const char *e = std::getenv("GEMM_GB300_SGEMM_PLAN")) {
-        if ((e[0] == 'L' || e[0] == 'S') && e[1] == ':') {
+        const CfgDesc *c = find_cfg(e[0]);
+        if (c != nullptr && e[1] == ':') {
             const int f = std::atoi(e + 2);
-            const bool l = e[0] == 'L';
-            if (f >= 1 && fits(l ? tiles_l : tiles_s, l ? CfgL::BM : CfgS::BM, l ? CfgL::BN : CfgS::BN, f))
-                plan = {e[0], f};
+            if (f >= 1 && fits(*c, f)) plan = {c, f};
         }
     }
     return plan;
@@ -103,25 +154,22 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     StreamWorkspace w;
     if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
         plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
-    const int bm = plan.cfg == 'L' ? CfgL::BM : CfgS::BM, bn = plan.cfg == 'L' ? CfgL::BN : CfgS::BN;
+    const CfgDesc &cfg = *plan.cfg;
     const int KT = static_cast<int>((K + 15) / 16);
-    const bool transposed = plan.cfg == 'L' ? KContigModes<CfgL>::kTransposed : KContigModes<CfgS>::kTransposed;
-    const int k_vec_a = transposed ? kKT : (a_vec ? kKVec : kKScalar);
-    const int k_vec_b = transposed ? kKT : (b_vec ? kKVec : kKScalar);
+    const int k_vec_a = cfg.transposed ? kKT : (a_vec ? kKVec : kKScalar);
+    const int k_vec_b = cfg.transposed ? kKT : (b_vec ? kKVec : kKScalar);
     const int a_mode = opA == GEMM_OP_N ? k_vec_a : (a_vec ? kMnVec : kMnScalar);
     const int b_mode = opB == GEMM_OP_T ? k_vec_b : (b_vec ? kMnVec : kMnScalar);
-    p.tiles_m = (M + bm - 1) / bm;
-    p.tiles_n = (N + bn - 1) / bn;
+    p.tiles_m = (M + cfg.bm - 1) / cfg.bm;
+    p.tiles_n = (N + cfg.bn - 1) / cfg.bn;
     p.splits = plan.splits;
     p.kt_per_split = (KT + plan.splits - 1) / plan.splits;
     if (plan.splits > 1) {
         p.ws = w.data;
         p.counters = w.counters;
-        return plan.cfg == 'L' ? launch_LS(dev.device, a_mode, b_mode, p, stream)
-                               : launch_SS(dev.device, a_mode, b_mode, p, stream);
+        return cfg.launch_split(dev.device, a_mode, b_mode, p, stream);
     }
-    return plan.cfg == 'L' ? launch_L(dev.device, a_mode, b_mode, p, stream)
-                           : launch_S(dev.device, a_mode, b_mode, p, stream);
+    return cfg.launch(dev.device, a_mode, b_mode, p, stream);
 }
 
 cudaError_t launch_scale_batched(int64_t M, int64_t N, float beta, float *C, int64_t ldc,

@@ -74,6 +74,7 @@ struct Cfg {
     static constexpr int M_STRIDE = BM / MB, N_STRIDE = BN / NB;
     static constexpr int A_STAGE = BK * BM, B_STAGE = BK * BN;  // floats per stage
     static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr bool PAIR_M = TM > TN;  // accumulator pairs along the longer side
     static_assert(TY * TX == kThreads, "one thread per TM x TN tile");
     static_assert(TX % 8 == 0 && TY % 4 == 0, "a warp covers 4 x 8 threads");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "128-bit fragment loads");
@@ -324,21 +325,80 @@ __device__ __forceinline__ void load_frag_mn(const float *stage, int k, int t4, 
     }
 }
 
-// [x][k] stages: the values at k and k+1 (k even: both in one 16-byte chunk), one 64-bit
-// load per row.
-template <int T, int STRIDE>
-__device__ __forceinline__ void load_frag_k_pair(const float *stage, int k, int t4, float (&v)[2][T])
+// [x][k] stages: the values at k .. k+G-1 (G = 2 or 4, k a multiple of G, so all of them
+// lie in one 16-byte chunk), one 64- or 128-bit load per row.
+template <int G, int T, int STRIDE>
+__device__ __forceinline__ void load_frag_k_group(const float *stage, int k, int t4, float (&v)[G][T])
 {
+    static_assert(G == 2 || G == 4, "k groups of 2 or 4");
 #pragma unroll
     for (int b = 0; b < T / 4; ++b)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int x = b * STRIDE + 4 * t4 + i;
-            const float2 f = *reinterpret_cast<const float2 *>(stage + swz_k(x, k));
-            v[0][4 * b + i] = f.x;
-            v[1][4 * b + i] = f.y;
+            if constexpr (G == 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(stage + swz_k(x, k));
+                v[0][4 * b + i] = f.x;
+                v[1][4 * b + i] = f.y;
+                v[2][4 * b + i] = f.z;
+                v[3][4 * b + i] = f.w;
+            } else {
+                const float2 f = *reinterpret_cast<const float2 *>(stage + swz_k(x, k));
+                v[0][4 * b + i] = f.x;
+                v[1][4 * b + i] = f.y;
+            }
         }
 }
+
+// The TM x TN accumulators of one thread, held as packed fp32 pairs for fma.rn.f32x2.
+// PAIR_M = false pairs neighbours along n (element (i, j) lives in v[i][j / 2]); PAIR_M = true
+// pairs neighbours along m (element (i, j) lives in v[i / 2][j]).  One operand of each packed
+// multiply-add is a pair straight out of a 128-bit fragment load; the other is a broadcast
+// value, which costs a register move, so the pairing follows the longer thread-tile side.
+template <int TM, int TN, bool PAIR_M>
+struct Acc {
+    static constexpr int R = PAIR_M ? TM / 2 : TM, S = PAIR_M ? TN : TN / 2;
+    float2 v[R][S];
+
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < S; ++c) v[r][c] = make_float2(0.f, 0.f);
+    }
+    __device__ __forceinline__ float &at(int i, int j)
+    {
+        if constexpr (PAIR_M) {
+            float2 &q = v[i >> 1][j];
+            return (i & 1) ? q.y : q.x;
+        } else {
+            float2 &q = v[i][j >> 1];
+            return (j & 1) ? q.y : q.x;
+        }
+    }
+    // acc += a b^T for one k (a: TM values along m, b: TN values along n).
+    __device__ __forceinline__ void fma(const float (&a)[TM], const float (&b)[TN])
+    {
+        if constexpr (PAIR_M) {
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const float2 bj = make_float2(b[j], b[j]);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    v[r][j] = __ffma2_rn(make_float2(a[2 * r], a[2 * r + 1]), bj, v[r][j]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                for (int c = 0; c < S; ++c)
+                    v[i][c] = __ffma2_rn(ai, make_float2(b[2 * c], b[2 * c + 1]), v[i][c]);
+            }
+        }
+    }
+};
 
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
@@ -409,12 +469,12 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         }
     }
 
-    float2 acc[C::TM][C::TN / 2];
-#pragma unroll
-    for (int i = 0; i < C::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < C::TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+    Acc<C::TM, C::TN, C::PAIR_M> acc;
+    acc.zero();
 
+    // K-major ([x][k]) operands are read KG consecutive k at a time, one 64- or 128-bit load per
+    // row; [k][x] operands one k at a time.
+    constexpr int KG = (!is_k_major(A_MODE) && !is_k_major(B_MODE)) ? 1 : (C::TM * C::TN <= 32 ? 4 : 2);
     for (int kt = 0; kt < KT; ++kt) {
         cp_async_wait<C::STAGES - 2>();
         __syncthreads();  // slice kt is visible; every thread is done with slot (kt-1)
@@ -424,51 +484,27 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 
         const float *As = sA + (kt % C::STAGES) * C::A_STAGE;
         const float *Bs = sB + (kt % C::STAGES) * C::B_STAGE;
-        if constexpr (!is_k_major(A_MODE) && !is_k_major(B_MODE)) {
-            // both operands [k][x]: one k at a time, 128-bit fragment reads
 #pragma unroll
-            for (int k = 0; k < C::BK; ++k) {
-                float a[C::TM], b[C::TN];
-                load_frag_mn<C::BM, C::TM, C::M_STRIDE>(As, k, ty, a);
-                load_frag_mn<C::BN, C::TN, C::N_STRIDE>(Bs, k, tx, b);
+        for (int k = 0; k < C::BK; k += KG) {
+            float ag[KG][C::TM], bg[KG][C::TN];
+            if constexpr (is_k_major(A_MODE)) load_frag_k_group<KG, C::TM, C::M_STRIDE>(As, k, ty, ag);
+            if constexpr (is_k_major(B_MODE)) load_frag_k_group<KG, C::TN, C::N_STRIDE>(Bs, k, tx, bg);
 #pragma unroll
-                for (int i = 0; i < C::TM; ++i) {
-                    const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-                    for (int j = 0; j < C::TN / 2; ++j)
-                        acc[i][j] = __ffma2_rn(ai, make_float2(b[2 * j], b[2 * j + 1]), acc[i][j]);
-                }
-            }
-            continue;
-        }
-#pragma unroll
-        for (int k = 0; k < C::BK; k += 2) {
-            // K-major operands come in k pairs; [k][m] / [k][n] operands one k at a time.
-            float a2[2][C::TM], b2[2][C::TN];
-            if constexpr (is_k_major(A_MODE)) load_frag_k_pair<C::TM, C::M_STRIDE>(As, k, ty, a2);
-            if constexpr (is_k_major(B_MODE)) load_frag_k_pair<C::TN, C::N_STRIDE>(Bs, k, tx, b2);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < KG; ++kk) {
                 float a[C::TM], b[C::TN];
                 if constexpr (is_k_major(A_MODE)) {
 #pragma unroll
-                    for (int i = 0; i < C::TM; ++i) a[i] = a2[kk][i];
+                    for (int i = 0; i < C::TM; ++i) a[i] = ag[kk][i];
                 } else {
                     load_frag_mn<C::BM, C::TM, C::M_STRIDE>(As, k + kk, ty, a);
                 }
                 if constexpr (is_k_major(B_MODE)) {
 #pragma unroll
-                    for (int j = 0; j < C::TN; ++j) b[j] = b2[kk][j];
+                    for (int j = 0; j < C::TN; ++j) b[j] = bg[kk][j];
                 } else {
                     load_frag_mn<C::BN, C::TN, C::N_STRIDE>(Bs, k + kk, tx, b);
                 }
-#pragma unroll
-                for (int i = 0; i < C::TM; ++i) {
-                    const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-                    for (int j = 0; j < C::TN / 2; ++j)
-                        acc[i][j] = __ffma2_rn(ai, make_float2(b[2 * j], b[2 * j + 1]), acc[i][j]);
-                }
+                acc.fma(a, b);
             }
         }
     }
@@ -485,8 +521,9 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         float4 *all = reinterpret_cast<float4 *>(p.ws) + tile * p.splits * tile4;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const float2 lo = acc[q / QR][2 * (q % QR)], hi = acc[q / QR][2 * (q % QR) + 1];
-            __stcg(all + split * tile4 + q * kThreads + tid, make_float4(lo.x, lo.y, hi.x, hi.y));
+            const int i = q / QR, j = 4 * (q % QR);
+            __stcg(all + split * tile4 + q * kThreads + tid,
+                   make_float4(acc.at(i, j), acc.at(i, j + 1), acc.at(i, j + 2), acc.at(i, j + 3)));
         }
         __threadfence();
         __shared__ unsigned int s_last;
@@ -506,12 +543,11 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const float4 u = __ldcg(all + s2 * tile4 + q * kThreads + tid);
-                float2 &lo = acc[q / QR][2 * (q % QR)], &hi = acc[q / QR][2 * (q % QR) + 1];
+                const int i = q / QR, j = 4 * (q % QR);
                 if (s2 == 0) {
-                    lo = make_float2(u.x, u.y);
-                    hi = make_float2(u.z, u.w);
+                    acc.at(i, j) = u.x; acc.at(i, j + 1) = u.y; acc.at(i, j + 2) = u.z; acc.at(i, j + 3) = u.w;
                 } else {
-                    lo.x += u.x; lo.y += u.y; hi.x += u.z; hi.y += u.w;
+                    acc.at(i, j) += u.x; acc.at(i, j + 1) += u.y; acc.at(i, j + 2) += u.z; acc.at(i, j + 3) += u.w;
                 }
             }
         }
@@ -531,8 +567,8 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 #pragma unroll
             for (int jb = 0; jb < C::NB; ++jb) {
                 const int64_t gn = col_of(jb);
-                const float2 lo = acc[i][2 * jb], hi = acc[i][2 * jb + 1];
-                float v[4] = {lo.x, lo.y, hi.x, hi.y};
+                const float v[4] = {acc.at(i, 4 * jb), acc.at(i, 4 * jb + 1), acc.at(i, 4 * jb + 2),
+                                    acc.at(i, 4 * jb + 3)};
                 if (p.c_vec && gn + 3 < p.N) {
                     float4 o;
                     if (beta != 0.0f) {
@@ -565,7 +601,6 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 #pragma unroll
             for (int jb = 0; jb < C::NB; ++jb) {
                 const int64_t gn = col_of(jb);
-                float2 &lo = acc[i][2 * jb], &hi = acc[i][2 * jb + 1];
                 float4 cin;
                 if (p.c_vec && gn + 3 < p.N) {
                     cin = *reinterpret_cast<const float4 *>(crow + gn);
@@ -575,20 +610,19 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
                     cin.z = gn + 2 < p.N ? crow[gn + 2] : 0.0f;
                     cin.w = gn + 3 < p.N ? crow[gn + 3] : 0.0f;
                 }
-                lo.x = fmaf(alpha, lo.x, beta * cin.x);
-                lo.y = fmaf(alpha, lo.y, beta * cin.y);
-                hi.x = fmaf(alpha, hi.x, beta * cin.z);
-                hi.y = fmaf(alpha, hi.y, beta * cin.w);
+                float &v0 = acc.at(i, 4 * jb), &v1 = acc.at(i, 4 * jb + 1);
+                float &v2 = acc.at(i, 4 * jb + 2), &v3 = acc.at(i, 4 * jb + 3);
+                v0 = fmaf(alpha, v0, beta * cin.x);
+                v1 = fmaf(alpha, v1, beta * cin.y);
+                v2 = fmaf(alpha, v2, beta * cin.z);
+                v3 = fmaf(alpha, v3, beta * cin.w);
             }
         }
     } else {
 #pragma unroll
         for (int i = 0; i < C::TM; ++i)
 #pragma unroll
-            for (int j = 0; j < C::TN / 2; ++j) {
-                acc[i][j].x *= alpha;
-                acc[i][j].y *= alpha;
-            }
+            for (int j = 0; j < C::TN; ++j) acc.at(i, j) *= alpha;
     }
 #pragma unroll
     for (int i = 0; i < C::TM; ++i) {
@@ -598,11 +632,11 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 #pragma unroll
         for (int jb = 0; jb < C::NB; ++jb) {
             const int64_t gn = col_of(jb);
-            const float2 lo = acc[i][2 * jb], hi = acc[i][2 * jb + 1];
+            const float v[4] = {acc.at(i, 4 * jb), acc.at(i, 4 * jb + 1), acc.at(i, 4 * jb + 2),
+                                acc.at(i, 4 * jb + 3)};
             if (p.c_vec && gn + 3 < p.N) {
-                *reinterpret_cast<float4 *>(crow + gn) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                *reinterpret_cast<float4 *>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
-                const float v[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
                     if (gn + jj < p.N) crow[gn + jj] = v[jj];
@@ -643,7 +677,7 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
     return cudaSuccess;
 }
 
-// Staging of K-contiguous operands per tile configuration: the 8 x 8 thread tile keeps the
+// Staging of K-contiguous operands per tile configuration: thread tiles 8 rows high keep the
 // 128-bit [k][x] fragment reads (transposing copies, kKT); the 4 x 4 thread tile stages
 // [x][k] with straight copies (kKVec / kKScalar).
 template <class C>
@@ -697,12 +731,16 @@ cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, 
 
 // Tile configurations (one translation unit each, see sgemm_cfg_*.cu).
 using CfgL = Cfg<128, 128, 16, 8, 8, 4, 2>;  // 8 x 8 per thread, two CTAs per SM
+using CfgM = Cfg<128, 64, 16, 8, 4, 4, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
 using CfgS = Cfg<64, 64, 16, 4, 4, 4, 3>;    // 4 x 4 per thread, three CTAs per SM
-static_assert(CfgL::BK == 16 && CfgS::BK == 16, "the host planner counts K in slices of 16");
+static_assert(CfgL::BK == 16 && CfgM::BK == 16 && CfgS::BK == 16,
+              "the host planner counts K in slices of 16");
 
 // Launchers defined in the configuration translation units.
 cudaError_t launch_L(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_LS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_M(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_MS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_S(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_SS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 

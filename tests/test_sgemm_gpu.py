@@ -84,6 +84,25 @@ def test_fuzz_shapes_ops_padding(opA, opB):
             assert torch.isnan(dev["C"][:, w.N:]).all()
 
 
+# Every tile configuration ('L' 128 x 128, 'M' 128 x 64, 'S' 64 x 64), with and without split K,
+# through the plan override, on shapes with ragged tails in M, N and K and both copy widths.
+@pytest.mark.parametrize("plan", ["L:1", "L:3", "M:1", "M:2", "M:5", "S:1", "S:3"])
+def test_every_tile_configuration(plan, monkeypatch):
+    monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", plan)
+    for i, (opA, opB) in enumerate(itertools.product("NT", "NT")):
+        for j, (M, N, K) in enumerate([(300, 200, 333), (129, 65, 160)]):
+            pad = (j, j, 0) if i % 2 == 0 else (0, 0, 3 * j)
+            w = workloads.Workload(f"plan{plan}_{M}x{N}x{K}_{opA}{opB}", "f32", M, N, K, opA,
+                                   opB, alpha=0.75, beta=0.5 if j == 0 else 0.0,
+                                   seed=200 + 4 * i + j, pad=pad)
+            inputs, dev = _run(w)
+            parity.check_full(w, inputs, dev["C"][:, : w.N].contiguous() if pad[2] else dev["C"])
+        wi = workloads.Workload(f"plan{plan}_int_{opA}{opB}", "f32", 257, 191, 515, opA, opB,
+                                seed=300 + i, dist_a="int4", dist_b="int4")
+        inputs, dev = _run(wi)
+        parity.check_full(wi, inputs, dev["C"], integer=True)
+
+
 @pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
 def test_integer_bit_exact_all_ops(opA, opB):
     w = workloads.Workload(f"int_{opA}{opB}", "f32", 300, 200, 1024, opA, opB, seed=7,
