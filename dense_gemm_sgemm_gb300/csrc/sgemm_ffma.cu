@@ -40,7 +40,7 @@ constexpr size_t kWsCounters = kWorkspaceCounters;
 struct CfgDesc {
     char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
     int bm, bn, min_blocks;
-    bool transposed;  // K-contiguous operands staged [k][x] (kKT)
+    bool a_k_major;  // a K-contiguous A is staged [x][k] (else transposed to [k][x])
     int max_splits;
     double us_slice;   // one K slice of one CTA, per co-resident CTA of the same SM
     double us_fixed;   // per wave of CTAs: prologue, epilogue, launch ramp
@@ -55,7 +55,7 @@ template <class C>
 constexpr CfgDesc desc(char name, int max_splits, double us_slice, double us_fixed, double us_split,
                        Launcher l, Launcher ls)
 {
-    return CfgDesc{name, C::BM, C::BN, C::MIN_BLOCKS, KContigModes<C>::kTransposed, max_splits,
+    return CfgDesc{name, C::BM, C::BN, C::MIN_BLOCKS, mode_allowed<C>(kKVec), max_splits,
                    us_slice, us_fixed, us_split, l, ls};
 }
 
@@ -156,10 +156,10 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
         plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
     const CfgDesc &cfg = *plan.cfg;
     const int KT = static_cast<int>((K + 15) / 16);
-    const int k_vec_a = cfg.transposed ? kKT : (a_vec ? kKVec : kKScalar);
-    const int k_vec_b = cfg.transposed ? kKT : (b_vec ? kKVec : kKScalar);
-    const int a_mode = opA == GEMM_OP_N ? k_vec_a : (a_vec ? kMnVec : kMnScalar);
-    const int b_mode = opB == GEMM_OP_T ? k_vec_b : (b_vec ? kMnVec : kMnScalar);
+    // K-contiguous operands (op(A) = N, op(B) = T): see mode_allowed
+    const int a_mode = opA == GEMM_OP_N ? (cfg.a_k_major ? (a_vec ? kKVec : kKScalar) : kKT)
+                                        : (a_vec ? kMnVec : kMnScalar);
+    const int b_mode = opB == GEMM_OP_T ? kKT : (b_vec ? kMnVec : kMnScalar);
     p.tiles_m = (M + cfg.bm - 1) / cfg.bm;
     p.tiles_n = (N + cfg.bn - 1) / cfg.bn;
     p.splits = plan.splits;

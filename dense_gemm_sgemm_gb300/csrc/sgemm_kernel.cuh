@@ -354,7 +354,7 @@ __device__ __forceinline__ void load_frag_k_group(const float *stage, int k, int
 // PAIR_M = false pairs neighbours along n (element (i, j) lives in v[i][j / 2]); PAIR_M = true
 // pairs neighbours along m (element (i, j) lives in v[i / 2][j]).  One operand of each packed
 // multiply-add is a pair straight out of a 128-bit fragment load; the other is a broadcast
-// value, which costs a register move, so the pairing follows the longer thread-tile side.
+// value, which costs register moves, so the pairing follows the longer thread-tile side.
 template <int TM, int TN, bool PAIR_M>
 struct Acc {
     static constexpr int R = PAIR_M ? TM / 2 : TM, S = PAIR_M ? TN : TN / 2;
@@ -677,32 +677,37 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
     return cudaSuccess;
 }
 
-// Staging of K-contiguous operands per tile configuration: thread tiles 8 rows high keep the
-// 128-bit [k][x] fragment reads (transposing copies, kKT); the 4 x 4 thread tile stages
-// [x][k] with straight copies (kKVec / kKScalar).
+// Staging modes each tile configuration is instantiated for: thread tiles 8 rows high keep
+// 128-bit [k][x] fragment reads (transposing copies of K-contiguous operands, kKT); the 4 x 4
+// tile stages a K-contiguous A [x][k] with straight copies (kKVec / kKScalar, read four k per
+// 128-bit load) and a K-contiguous B through transposing copies (kKT: [x][k] reads of B rows
+// 4t .. 4t+3 would fall into the same 16 banks).
 template <class C>
-struct KContigModes {
-    static constexpr bool kTransposed = C::TM >= 8;
-};
+constexpr bool mode_allowed(int mode)
+{
+    if (C::TM >= 8) return mode == kMnVec || mode == kMnScalar || mode == kKT;
+    return mode == kMnVec || mode == kMnScalar || mode == kKVec || mode == kKScalar || mode == kKT;
+}
+
+template <class C, bool SPLIT, int A_MODE, int B_MODE>
+cudaError_t launch_if_allowed(int dev_id, const SgemmParams &p, cudaStream_t s)
+{
+    if constexpr (mode_allowed<C>(A_MODE) && mode_allowed<C>(B_MODE))
+        return launch_cfg<C, SPLIT, A_MODE, B_MODE>(dev_id, p, s);
+    else
+        return cudaErrorInvalidValue;
+}
 
 template <class C, bool SPLIT, int A_MODE>
 cudaError_t launch_b(int dev_id, int b_mode, const SgemmParams &p, cudaStream_t s)
 {
-    if constexpr (KContigModes<C>::kTransposed) {
-        switch (b_mode) {
-        case kMnVec: return launch_cfg<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
-        case kMnScalar: return launch_cfg<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
-        case kKT: return launch_cfg<C, SPLIT, A_MODE, kKT>(dev_id, p, s);
-        default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (b_mode) {
-        case kMnVec: return launch_cfg<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
-        case kMnScalar: return launch_cfg<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
-        case kKVec: return launch_cfg<C, SPLIT, A_MODE, kKVec>(dev_id, p, s);
-        case kKScalar: return launch_cfg<C, SPLIT, A_MODE, kKScalar>(dev_id, p, s);
-        default: return cudaErrorInvalidValue;
-        }
+    switch (b_mode) {
+    case kMnVec: return launch_if_allowed<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
+    case kMnScalar: return launch_if_allowed<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
+    case kKVec: return launch_if_allowed<C, SPLIT, A_MODE, kKVec>(dev_id, p, s);
+    case kKScalar: return launch_if_allowed<C, SPLIT, A_MODE, kKScalar>(dev_id, p, s);
+    case kKT: return launch_if_allowed<C, SPLIT, A_MODE, kKT>(dev_id, p, s);
+    default: return cudaErrorInvalidValue;
     }
 }
 
@@ -711,21 +716,14 @@ cudaError_t launch_b(int dev_id, int b_mode, const SgemmParams &p, cudaStream_t 
 template <class C, bool SPLIT>
 cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s)
 {
-    if constexpr (KContigModes<C>::kTransposed) {
-        switch (a_mode) {
-        case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
-        case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
-        case kKT: return launch_b<C, SPLIT, kKT>(dev_id, b_mode, p, s);
-        default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (a_mode) {
-        case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
-        case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
-        case kKVec: return launch_b<C, SPLIT, kKVec>(dev_id, b_mode, p, s);
-        case kKScalar: return launch_b<C, SPLIT, kKScalar>(dev_id, b_mode, p, s);
-        default: return cudaErrorInvalidValue;
-        }
+    if (!mode_allowed<C>(a_mode)) return cudaErrorInvalidValue;
+    switch (a_mode) {
+    case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
+    case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
+    case kKVec: return launch_b<C, SPLIT, kKVec>(dev_id, b_mode, p, s);
+    case kKScalar: return launch_b<C, SPLIT, kKScalar>(dev_id, b_mode, p, s);
+    case kKT: return launch_b<C, SPLIT, kKT>(dev_id, b_mode, p, s);
+    default: return cudaErrorInvalidValue;
     }
 }
 
