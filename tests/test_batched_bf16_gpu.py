@@ -119,6 +119,15 @@ def test_sgemm_strided_batched_shared_operand_and_split_k():
     _check_batched(_batched_case("f32", 4, 200, 64, 513, "T", "N", share_b=True, beta=0.0, seed=3))
 
 
+@pytest.mark.parametrize("share", ["none", "a", "b"])
+def test_sgemm_strided_batched_transposed_first(share, monkeypatch):
+    # large enough for the transposition of K-contiguous operands into scratch (see
+    # test_sgemm_gpu); a shared operand is transposed once
+    monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", "L:1")
+    _check_batched(_batched_case("f32", 2, 2050, 2049, 600, "N", "T", share_a=share == "a",
+                                 share_b=share == "b", seed=4))
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("opA,opB", [("N", "N"), ("N", "T"), ("T", "N")])
 def test_tensor_core_strided_batched(dtype, opA, opB):

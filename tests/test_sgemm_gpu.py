@@ -103,6 +103,19 @@ def test_every_tile_configuration(plan, monkeypatch):
         parity.check_full(wi, inputs, dev["C"], integer=True)
 
 
+# Large problems on the 128-row tiles transpose a K-contiguous operand into scratch first
+# (op(A) = N when N >= 2048, op(B) = T when M >= 2048, at 1e10 flops or more): unaligned
+# leading dimensions, ragged K and both operands at once.
+@pytest.mark.parametrize("opA,opB", [("N", "N"), ("N", "T"), ("T", "T")])
+def test_large_k_contiguous_operands_are_transposed_first(opA, opB, monkeypatch):
+    monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", "L:1")
+    w = workloads.Workload(f"pretranspose_{opA}{opB}", "f32", 3100, 3079, 531, opA, opB,
+                           alpha=0.5, beta=0.25, seed=31, pad=(1, 3, 0), dist_a="int4",
+                           dist_b="int4", dist_c="int4")
+    inputs, dev = _run(w)
+    parity.check_full(w, inputs, dev["C"], integer=True)
+
+
 @pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
 def test_integer_bit_exact_all_ops(opA, opB):
     w = workloads.Workload(f"int_{opA}{opB}", "f32", 300, 200, 1024, opA, opB, seed=7,
