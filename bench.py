@@ -142,22 +142,34 @@ def whole_job_value(local_total_ms, steps, flops_per_step, world, device=None):
     return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12, total_ms
 
 
-def csrc_digest() -> str:
-    """First 16 hex digits of a sha256 over every CUDA source of the library."""
+# The CUDA sources each profiled kernel is built from (its launch planning included).
+KERNEL_SOURCES = {
+    "sgemm_ffma": ("sgemm_*", "gemm_internal.h"),
+    "hgemm_tcgen05": ("hgemm_tcgen05.cu", "gemm_internal.h"),
+}
+
+
+def csrc_digest(kernel: str) -> str:
+    """First 16 hex digits of a sha256 over the CUDA sources of one kernel (file names and
+    contents, in name order)."""
     import glob
 
+    paths = set()
+    for pattern in KERNEL_SOURCES[kernel]:
+        paths.update(glob.glob(os.path.join(ROOT, "dense_gemm_sgemm_gb300", "csrc", pattern)))
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "dense_gemm_sgemm_gb300", "csrc", "*"))):
+    for path in sorted(paths):
         h.update(os.path.basename(path).encode())
         h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(profile: str):
-    """DRAM bytes per launch from a committed ncu summary, if the sources are unchanged."""
+def _traffic_from_profile(kernel: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are
+    unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", profile)
     try:
-        digest = csrc_digest()
+        digest = csrc_digest(kernel)
         fields = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
@@ -351,7 +363,7 @@ def run_ours(args, rank, world, local):
         kernel = "hgemm_tcgen05"
         bound, peak = "tensor", peaks["bf16_tflops"]
         peak_src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
-    traffic = _traffic_from_profile(f"{kernel}_{w.name}.txt")
+    traffic = _traffic_from_profile(kernel, f"{kernel}_{w.name}.txt")
     vs = (round(value / (PAGES_RAGGED_GFLOPS / 1e3), 4)
           if w.name == workloads.sgemm_ragged().name else None)
     line = {

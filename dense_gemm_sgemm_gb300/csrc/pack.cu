@@ -84,24 +84,33 @@ void *pack_buffer(int dev, cudaStream_t stream, int which, size_t bytes)
     return p;
 }
 
-// dst[b][c][r] = src[b][r][c] through a 32 x 33 shared tile: 128-byte row reads of src and
-// 128-byte row writes of dst.  Columns r >= rows of dst (row padding) are left unwritten.
-__global__ void transpose_f32(const float *__restrict__ src, int64_t ld, int64_t stride,
-                              float *__restrict__ dst, int64_t ldt, int64_t stride_t, int64_t rows,
-                              int64_t cols)
+// dst[b][c][r] = src[b][r][c] through a 64 x 65 shared tile, 256 threads: each thread issues
+// its 16 loads (rows ty + 4i of one column) before any store, so enough reads are in flight
+// to keep HBM busy; reads and writes are 128-byte row segments per warp.  Columns r >= rows
+// of dst (row padding) are left unwritten.
+constexpr int kTT = 64;
+__global__ void __launch_bounds__(256) transpose_f32(const float *__restrict__ src, int64_t ld, int64_t stride,
+                                                     float *__restrict__ dst, int64_t ldt, int64_t stride_t,
+                                                     int64_t rows, int64_t cols)
 {
-    __shared__ float tile[32][33];
-    const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
+    __shared__ float tile[kTT][kTT + 1];
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+    const int64_t r0 = int64_t(blockIdx.y) * kTT, c0 = int64_t(blockIdx.x) * kTT;
     const float *s = src + int64_t(blockIdx.z) * stride;
     float *d = dst + int64_t(blockIdx.z) * stride_t;
-    for (int i = threadIdx.y; i < 32; i += 8) {
-        const int64_t r = r0 + i, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) tile[i][threadIdx.x] = s[r * ld + c];
+    float v[kTT / 4];
+#pragma unroll
+    for (int i = 0; i < kTT / 4; ++i) {
+        const int64_t r = r0 + ty + 4 * i, c = c0 + tx;
+        v[i] = r < rows && c < cols ? __ldg(s + r * ld + c) : 0.0f;
     }
+#pragma unroll
+    for (int i = 0; i < kTT / 4; ++i) tile[ty + 4 * i][tx] = v[i];
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += 8) {
-        const int64_t c = c0 + i, r = r0 + threadIdx.x;
-        if (c < cols && r < rows) d[c * ldt + r] = tile[threadIdx.x][i];
+#pragma unroll
+    for (int i = 0; i < kTT / 4; ++i) {
+        const int64_t c = c0 + ty + 4 * i, r = r0 + tx;
+        if (c < cols && r < rows) d[c * ldt + r] = tile[tx][ty + 4 * i];
     }
 }
 
@@ -113,7 +122,7 @@ bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float 
 {
     const int64_t ldt = (rows + 3) / 4 * 4;
     const int64_t nb = stride == 0 ? 1 : batch;  // a shared operand is transposed once
-    const int64_t grid_y = (rows + 31) / 32, grid_x = (cols + 31) / 32;
+    const int64_t grid_y = (rows + kTT - 1) / kTT, grid_x = (cols + kTT - 1) / kTT;
     if (grid_y > 65535 || grid_x > 0x7fffffff) return false;
     const size_t bytes = size_t(nb) * size_t(cols) * size_t(ldt) * 4;
     float *dst = static_cast<float *>(pack_buffer(dev, stream, which, bytes > 0 ? bytes : 16));
@@ -121,7 +130,7 @@ bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float 
     for (int64_t b0 = 0; b0 < nb; b0 += 65535) {
         const int64_t nz = nb - b0 < 65535 ? nb - b0 : 65535;
         const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(grid_y), static_cast<unsigned>(nz));
-        transpose_f32<<<grid, dim3(32, 8), 0, stream>>>(src + b0 * stride, ld, stride, dst + b0 * cols * ldt, ldt,
+        transpose_f32<<<grid, 256, 0, stream>>>(src + b0 * stride, ld, stride, dst + b0 * cols * ldt, ldt,
                                                         cols * ldt, rows, cols);
         if (cudaGetLastError() != cudaSuccess) return false;
     }
