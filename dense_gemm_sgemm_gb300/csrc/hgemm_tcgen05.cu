@@ -16,8 +16,12 @@
 //               accumulators), issues 4 tcgen05.mma (M=128, N=256, K=16) per slice and
 //               returns each slice to the producer with tcgen05.commit;
 //   warps 2-5   epilogue: tcgen05.ld the finished accumulator (one TMEM lane = one row of
-//               the tile), apply C = alpha * acc + beta * C and store with 128-bit stores,
+//               the tile), pass each 32 x 32 piece through a shared staging tile so that
+//               C = alpha * acc + beta * C is read and written in 128-byte row segments,
 //               while warp 1 already accumulates the next tile into the other buffer.
+//
+// The last, partial wave of tiles is split so that more SMs share it: into K halves whose
+// fp32 partial tiles are added by the half that finishes second, or into N halves.
 //
 // Tiles are visited in the grouped raster of the copecc "线程块网格重排" section.  Ragged M,
 // N and K need no special code: TMA fills out-of-range elements with zeros, which add
@@ -50,8 +54,9 @@ constexpr int kTmemCols = 2 * BN;   // two accumulators
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int EPI_BYTES = 4 * 32 * 32 * 4;  // a 32 x 32 fp32 staging tile per epilogue warp
 constexpr int kBarBytes = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kBarBytes + 1024;  // + alignment slack
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
 constexpr int kLogGroup = 3;
 
 struct HgemmParams {
@@ -64,12 +69,20 @@ struct HgemmParams {
     int c_vec;               // C base 16-byte aligned and ldc % 4 == 0
     uint64_t timeout_ns;     // limit of every barrier wait
     int inject_stall;        // test hook: the producer never fills the first slice
-    // Work units.  Units [0, full_tiles) are whole 128 x 256 tiles.  When tail_halves is set,
-    // each tile of the last, partial wave becomes two units of 128 x 128 (left and right
-    // half), so twice as many SMs share that wave.  Every output element is still summed by
-    // one CTA over all of K in the same order, so the split changes no result bit.
+    // Work units.  Units [0, full_tiles) are whole 128 x 256 tiles over all of K.  Each tile
+    // of the last, partial wave becomes two units, so twice as many SMs share that wave:
+    //   tail_mode kTailN: the left and right 128 x 128 halves (every element still summed by
+    //     one CTA over all of K, so no result bit changes);
+    //   tail_mode kTailK: the first and second half of the K slices.  Each half stores its
+    //     fp32 partial tile in ws; the half that finishes second (counted in counters) adds
+    //     the other's partial to its own and writes C.  Two fp32 values sum to the same bits
+    //     in either order, so the result does not depend on which half finishes first.
+    // Every K slice costs the ring's round-trip latency whatever the unit's width, so K
+    // halves finish the wave in half the time and N halves do not.
     int64_t full_tiles, num_units;
-    int tail_halves;
+    int tail_mode;
+    float *ws;               // kTailK: 2 partial tiles per split tile (per CTA of a cluster)
+    unsigned int *counters;  // kTailK: one arrival counter per split tile, zero between launches
     // Strided batch: batch problems share M, N, K; work units count tiles (or tile pairs)
     // of every problem, problem b owning units [b * per_batch, (b + 1) * per_batch).
     int64_t batch, per_batch;
@@ -78,19 +91,34 @@ struct HgemmParams {
     uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
 };
 
-// Tile, column offset within it and width of work unit u.
-__device__ __forceinline__ void decode_unit(const HgemmParams &p, int64_t u, int64_t &t, int &n_off, int &width)
+constexpr int kTailNone = 0, kTailN = 1, kTailK = 2;
+
+// Work unit u: tile t, column offset and width within it, K slices [kb0, kb1), and for a
+// K-half unit its half (0 or 1) and the index of its tile among the split tiles (else -1).
+struct Unit {
+    int64_t t, split_slot;
+    int n_off, width, kb0, kb1, khalf;
+};
+
+__device__ __forceinline__ Unit decode_unit(const HgemmParams &p, int64_t u)
 {
-    if (u < p.full_tiles || !p.tail_halves) {
-        t = u;
-        n_off = 0;
-        width = BN;
-    } else {
+    Unit x{u, -1, 0, BN, 0, p.num_kb, -1};
+    if (u >= p.full_tiles && p.tail_mode != kTailNone) {
         const int64_t r = u - p.full_tiles;
-        t = p.full_tiles + (r >> 1);
-        n_off = static_cast<int>(r & 1) * (BN / 2);
-        width = BN / 2;
+        const int h = static_cast<int>(r & 1);
+        x.t = p.full_tiles + (r >> 1);
+        if (p.tail_mode == kTailN) {
+            x.n_off = h * (BN / 2);
+            x.width = BN / 2;
+        } else {
+            const int mid = p.num_kb / 2;
+            x.kb0 = h ? mid : 0;
+            x.kb1 = h ? p.num_kb : mid;
+            x.khalf = h;
+            x.split_slot = r >> 1;
+        }
     }
+    return x;
 }
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -149,6 +177,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
             if (global_timer_ns() - t0 > timeout_ns) return false;
         }
     }
+}
+
+// OR of `pred` over the 128 threads of the four epilogue warps (named barrier 1); every one
+// of them must call it.
+__device__ __forceinline__ bool epilogue_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int *abort_flag)
@@ -306,7 +350,8 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
 
     const uint32_t sA = base;                          // STAGES x 16 KB
     const uint32_t sB = base + STAGES * A_STAGE_BYTES; // STAGES x 32 KB
-    uint8_t *bar_area = smem + STAGES * STAGE_BYTES;
+    float4 *epi_tiles = reinterpret_cast<float4 *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *bar_area = smem + STAGES * STAGE_BYTES + EPI_BYTES;
     const uint32_t bar0 = smem_u32(bar_area);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -366,9 +411,10 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             uint32_t filled = 0, fill_parity = 0;  // per stage: a fill was issued / its parity
             bool ok = true;
             for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
-                int64_t t, tm, tn;
-                int n_off, width;
-                decode_unit(p, u, t, n_off, width);
+                const Unit x = decode_unit(p, u);
+                const int64_t t = x.t;
+                const int n_off = x.n_off, width = x.width;
+                int64_t tm, tn;
                 const int64_t bt = t / p.per_batch;
                 raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
                 if (MC) tm = 2 * tm + rank;
@@ -377,7 +423,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 const int32_t m0 = static_cast<int32_t>(tm * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off;
                 const uint32_t bytes = A_STAGE_BYTES + uint32_t(width) * BK * 2;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
                         raise_abort(abort_flag);
                         ok = false;
@@ -387,7 +433,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     mbar_expect_tx(fb, bytes);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    const bool stall = p.inject_stall && u == unit0 && kb == 0;
+                    const bool stall = p.inject_stall && u == unit0 && kb == x.kb0;
                     if (!stall) {
                         const int32_t k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
@@ -455,17 +501,15 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
             for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
-                int64_t t;
-                int n_off, width;
-                decode_unit(p, u, t, n_off, width);
-                const uint32_t idesc = width == BN ? idesc_full : idesc_half;
+                const Unit x = decode_unit(p, u);
+                const uint32_t idesc = x.width == BN ? idesc_full : idesc_half;
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, tmo)) {
                     raise_abort(abort_flag);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, tmo)) {
                         raise_abort(abort_flag);
                         ok = false;
@@ -482,7 +526,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                                                  : smem_desc(a_tile + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc(b_tile + k * 2048, 8192, 1024)
                                                  : smem_desc(b_tile + k * 32, 16, 1024);
-                        umma_f16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_f16(d_tmem, ad, bd, idesc, (kb > x.kb0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
                     // slot free once these MMAs have read it (MC: in both CTAs' counts)
@@ -504,63 +548,130 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     } else {
         // ---------------- epilogue (warps 2..5; TMEM lane quarter = warp % 4)
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         const float alpha = p.alpha, beta = p.beta;
         for (int64_t u = unit0; u < p.num_units; u += ustride) {
-            int64_t t, tm, tn;
-            int n_off, width;
-            decode_unit(p, u, t, n_off, width);
+            const Unit x = decode_unit(p, u);
+            const int64_t t = x.t;
+            const int n_off = x.n_off, width = x.width;
+            int64_t tm, tn;
             const int64_t bt = t / p.per_batch;
             raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
             if (MC) tm = 2 * tm + rank;
-            if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo)) {
+            // The four epilogue warps leave together or not at all: a K-half unit below
+            // synchronises them, so none may have given up on a unit the others continue.
+            const bool got = mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo);
+            if (epilogue_any(!got)) {
                 raise_abort(abort_flag);
                 break;
             }
             tc_fence_after();
-            const int64_t gm = tm * BM + row;
-            const bool row_ok = gm < p.M;
-            float *crow = p.C + bt * p.stride_c + (row_ok ? gm * p.ldc : 0);
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
-#pragma unroll 1
-            for (int c = 0; c < width / 32; ++c) {
-                float v[32];
-                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the predicated stores
-                tmem_ld_32(taddr + c * 32, v);
+            // C = alpha * acc + beta * C for chunk c (32 columns) of the warp's 32 rows; v holds
+            // this lane's row.  The rows go through the warp's staging tile (16-byte chunks
+            // XOR-swizzled by row: conflict-free both ways), so that each store instruction
+            // writes four 128-byte row segments instead of 32 scattered 16-byte pieces.
+            float4 *tile = epi_tiles + quarter * 256;
+            const int64_t row0 = tm * BM + quarter * 32;  // first row of this warp
+            auto store_chunk = [&](int c, float (&v)[32]) {
                 const int64_t gn0 = tn * BN + n_off + c * 32;
-                if (!row_ok || gn0 >= p.N) continue;
-                if (p.c_vec && gn0 + 32 <= p.N) {
-                    float4 *dst = reinterpret_cast<float4 *>(crow + gn0);
-                    if (beta != 0.0f) {  // all eight reads of C in flight before any store
-                        float4 ci[8];
+                if (gn0 >= p.N) return;  // the same for the whole warp
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) ci[j] = dst[j];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(fmaf(alpha, v[4 * j + 0], beta * ci[j].x),
-                                                 fmaf(alpha, v[4 * j + 1], beta * ci[j].y),
-                                                 fmaf(alpha, v[4 * j + 2], beta * ci[j].z),
-                                                 fmaf(alpha, v[4 * j + 3], beta * ci[j].w));
+                for (int j = 0; j < 8; ++j)
+                    tile[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                __syncwarp();
+                const int q = lane & 7;
+                const int64_t gn = gn0 + 4 * q;
+                const bool vec = p.c_vec && gn + 3 < p.N;
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + (lane >> 3);
+                    const int64_t gm = row0 + r;
+                    const float4 a = tile[r * 8 + (q ^ (r & 7))];
+                    if (gm >= p.M) continue;
+                    float *dst = p.C + bt * p.stride_c + gm * p.ldc + gn;
+                    if (vec) {
+                        float4 o;
+                        if (beta != 0.0f) {
+                            const float4 ci = *reinterpret_cast<const float4 *>(dst);
+                            o = make_float4(fmaf(alpha, a.x, beta * ci.x), fmaf(alpha, a.y, beta * ci.y),
+                                            fmaf(alpha, a.z, beta * ci.z), fmaf(alpha, a.w, beta * ci.w));
+                        } else {
+                            o = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
+                        }
+                        *reinterpret_cast<float4 *>(dst) = o;
                     } else {
+                        const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(alpha * v[4 * j], alpha * v[4 * j + 1], alpha * v[4 * j + 2],
-                                                 alpha * v[4 * j + 3]);
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (gn + jj < p.N)
+                                dst[jj] = beta != 0.0f ? fmaf(alpha, av[jj], beta * dst[jj]) : alpha * av[jj];
                     }
-                } else {
-                    if (beta != 0.0f) {  // reads first, then stores
+                }
+                __syncwarp();  // the tile is read before the next chunk overwrites it
+            };
+            if (x.khalf < 0) {
+#pragma unroll 1
+                for (int c = 0; c < width / 32; ++c) {
+                    float v[32];
+                    __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the predicated stores
+                    tmem_ld_32(taddr + c * 32, v);
+                    store_chunk(c, v);
+                }
+            } else {
+                // K half: publish this half's partial tile, count the arrival; the half that
+                // arrives second adds the other partial and writes C.  Partials are stored
+                // thread-major (float4 q of epilogue thread e at q * 128 + e), so every warp
+                // access is 512 contiguous bytes.  The second half copies the other partial
+                // into the operand ring, idle now (a split unit is its CTA's last unit and
+                // every load into the ring has landed), with 16-byte cp.async.
+                const int e = threadIdx.x - 64;
+                const int64_t slot = MC ? 2 * x.split_slot + rank : x.split_slot;
+                constexpr int Q = BN / 4;  // float4 per row
+                float4 *mine = reinterpret_cast<float4 *>(p.ws) + (slot * 2 + x.khalf) * (Q * 128) + e;
+                const float4 *other = reinterpret_cast<const float4 *>(p.ws) + (slot * 2 + (x.khalf ^ 1)) * (Q * 128) + e;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld_32(taddr + c * 32, v);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = fmaf(alpha, v[j], gn0 + j < p.N ? beta * crow[gn0 + j] : 0.0f);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(mine + (c * 8 + j) * 128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps' partials
+                bool arrived_second = false;
+                if (threadIdx.x == 64) {
+                    __threadfence();  // release this CTA's partial (cumulative over the barrier)
+                    arrived_second = atomicAdd(p.counters + slot, 1u) == 1u;
+                    if (arrived_second) {
+                        p.counters[slot] = 0;  // ready for the next launch
+                        __threadfence();       // acquire the other half's partial
                     }
+                }
+                if (epilogue_any(arrived_second)) {
+                    static_assert(Q * 128 * 16 <= STAGES * STAGE_BYTES, "the ring holds a partial tile");
+                    const uint32_t stage_dst = sA + uint32_t(e) * 16u;
+#pragma unroll 8
+                    for (int q = 0; q < Q; ++q)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stage_dst + uint32_t(q) * 2048u),
+                                     "l"(other + q * 128)
+                                     : "memory");
+                    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+                    const float4 *staged = reinterpret_cast<const float4 *>(smem) + e;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float v[32];
+                        __syncwarp();
+                        tmem_ld_32(taddr + c * 32, v);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (gn0 + j < p.N) crow[gn0 + j] = v[j];
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 o = staged[(c * 8 + j) * 128];
+                            v[4 * j] += o.x; v[4 * j + 1] += o.y; v[4 * j + 2] += o.z; v[4 * j + 3] += o.w;
+                        }
+                        store_chunk(c, v);
+                    }
                 }
             }
             tc_fence_before();
@@ -669,7 +780,9 @@ template <int A_MN, int B_MN>
 cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaStream_t stream)
 {
     const char *no_mc = std::getenv("GEMM_GB300_HGEMM_NO_MULTICAST");
-    const char *no_halves = std::getenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES");
+    // GEMM_GB300_HGEMM_TAIL: "0" no tail split, "n" N halves, otherwise the rule below
+    const char *tail_env = std::getenv("GEMM_GB300_HGEMM_TAIL");
+    const char tail_want = tail_env && tail_env[0] ? tail_env[0] : 'a';
     bool mc = p.tiles_m >= 2 && !(no_mc && no_mc[0] == '1');
     int max_clusters = 0;
     if (mc) {
@@ -678,19 +791,31 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         mc = max_clusters > 0;
     }
     // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
-    // half of the workers idle, its tiles are processed as two half-width units each.
+    // half of the workers idle, its tiles are split in two units each: K halves when there
+    // are at least 8 K slices and the stream's workspace holds the partial tiles, else N
+    // halves.
     p.per_batch = mc ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
     const int64_t work = p.per_batch * p.batch;
     const int64_t workers_max = mc ? max_clusters : dev.num_sms;
     const int64_t workers = work < workers_max ? work : workers_max;
     p.full_tiles = work;
     p.num_units = work;
-    p.tail_halves = 0;
+    p.tail_mode = kTailNone;
     const int64_t full = (work / workers) * workers, tail = work - full;
-    if (tail > 0 && 2 * tail <= workers && !(no_halves && no_halves[0] == '1')) {
+    if (tail > 0 && 2 * tail <= workers && tail_want != '0') {
+        const int64_t split_tiles = tail * (mc ? 2 : 1);  // CTA tiles of the split units
+        StreamWorkspace w;
+        if (tail_want != 'n' && p.num_kb >= 8 && split_tiles <= int64_t(kWorkspaceCounters) &&
+            size_t(split_tiles) * 2 * BM * BN * sizeof(float) <= kWorkspaceBytes &&
+            stream_workspace(dev.device, stream, w)) {
+            p.tail_mode = kTailK;
+            p.ws = w.data;
+            p.counters = w.counters;
+        } else {
+            p.tail_mode = kTailN;
+        }
         p.full_tiles = full;
         p.num_units = full + 2 * tail;
-        p.tail_halves = 1;
     }
     if (!mc) {
         cudaError_t e = set_smem_attr<A_MN, B_MN, false>(dev.device);

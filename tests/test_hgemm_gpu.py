@@ -137,9 +137,25 @@ def test_beta_zero_ignores_nan():
     assert torch.isfinite(C).all()
 
 
-def test_tail_wave_half_width_units_full_oracle():
-    # 18 x 10 = 180 tiles of 128 x 256: 152 run whole, and each of the 28 tiles of the last
-    # wave runs as two 128 x 128 units on different SMs.
+# The last, partial wave of tiles is split in two units per tile: K halves by default (at
+# least 8 K slices; the half that finishes second adds the other's fp32 partial), N halves
+# through GEMM_GB300_HGEMM_TAIL=n, none with GEMM_GB300_HGEMM_TAIL=0.
+TAIL_MODES = ["auto", "n"]
+
+
+def _tail_env(monkeypatch, mode, multicast=True):
+    if mode != "auto":
+        monkeypatch.setenv("GEMM_GB300_HGEMM_TAIL", mode)
+    if not multicast:
+        monkeypatch.setenv("GEMM_GB300_HGEMM_NO_MULTICAST", "1")
+
+
+@pytest.mark.parametrize("multicast", [True, False])
+@pytest.mark.parametrize("mode", TAIL_MODES)
+def test_tail_wave_split_units_full_oracle(mode, multicast, monkeypatch):
+    # 18 x 10 = 180 tiles of 128 x 256 (90 pairs with two-CTA clusters): the tiles of the last
+    # wave run as two units each on different SMs.
+    _tail_env(monkeypatch, mode, multicast)
     w = workloads.Workload("hgemm_tail_2300x2560x512", "f16", 2300, 2560, 512, alpha=0.75,
                            beta=0.5, seed=12, pad=(0, 0, 3))
     inputs, dev = _run(w)
@@ -147,21 +163,43 @@ def test_tail_wave_half_width_units_full_oracle():
     assert torch.isnan(dev["C"][:, w.N:]).all()
 
 
+@pytest.mark.parametrize("mode", TAIL_MODES)
 @pytest.mark.parametrize("opB", ["N", "T"])
-def test_tail_wave_half_width_units_integer_bit_exact(opB):
-    w = workloads.Workload(f"hgemm_tail_int_{opB}", "f16", 2304, 2600, 512, opB=opB, seed=13,
+def test_tail_wave_split_units_integer_bit_exact(opB, mode, monkeypatch):
+    _tail_env(monkeypatch, mode)
+    w = workloads.Workload(f"hgemm_tail_int_{opB}", "f16", 2304, 2600, 1000, opB=opB, seed=13,
                            dist_a="int4", dist_b="int4", pad=(0, (-2600) % 8 if opB == "N" else 0, 0))
     inputs, dev = _run(w)
     parity.check_full(w, inputs, dev["C"], integer=True)
 
 
-def test_tail_half_units_change_no_bit(monkeypatch):
+def test_tail_n_halves_change_no_bit(monkeypatch):
     # Each output element is summed by one CTA over all of K either way.
     w = workloads.Workload("hgemm_tail_same_bits", "f16", 2304, 2560, 640, seed=14)
+    monkeypatch.setenv("GEMM_GB300_HGEMM_TAIL", "n")
     inputs, dev = _run(w)
     with_halves = dev["C"].clone()
-    monkeypatch.setenv("GEMM_GB300_HGEMM_NO_TAIL_HALVES", "1")
+    monkeypatch.setenv("GEMM_GB300_HGEMM_TAIL", "0")
     dev["C"].copy_(inputs["C"].cuda())
     parity.run_library(w, dev)
     torch.cuda.synchronize()
     assert torch.equal(with_halves.view(torch.int32), dev["C"].view(torch.int32))
+
+
+def test_tail_k_halves_deterministic_and_counters_reset():
+    # Whichever K half finishes second, the two partials sum to the same bits; the arrival
+    # counters are back at zero after every launch, so repeated launches agree.
+    w = workloads.Workload("hgemm_tail_k_repeat", "f16", 2304, 2560, 640, alpha=1.0, beta=1.0,
+                           seed=15)
+    inputs = workloads.make_inputs(w)
+    dev = parity.to_device(inputs)
+    outs = []
+    for _ in range(4):
+        dev["C"].copy_(inputs["C"].cuda())
+        parity.run_library(w, dev)
+        torch.cuda.synchronize()
+        assert gemm_get_device_status() == 0
+        outs.append(dev["C"].clone())
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    parity.check_sampled(w, inputs, outs[0], n_random=2048)
