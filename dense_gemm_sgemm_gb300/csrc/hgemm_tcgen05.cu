@@ -584,19 +584,29 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 const int q = lane & 7;
                 const int64_t gn = gn0 + 4 * q;
                 const bool vec = p.c_vec && gn + 3 < p.N;
-#pragma unroll 2
+                float *cbase = p.C + bt * p.stride_c + gn;
+                // every read of C in flight before the first store
+                float4 ci[8];
+                if (vec && beta != 0.0f) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int64_t gm = row0 + 4 * i + (lane >> 3);
+                        ci[i] = gm < p.M ? *reinterpret_cast<const float4 *>(cbase + gm * p.ldc)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = 4 * i + (lane >> 3);
                     const int64_t gm = row0 + r;
                     const float4 a = tile[r * 8 + (q ^ (r & 7))];
                     if (gm >= p.M) continue;
-                    float *dst = p.C + bt * p.stride_c + gm * p.ldc + gn;
+                    float *dst = cbase + gm * p.ldc;
                     if (vec) {
                         float4 o;
                         if (beta != 0.0f) {
-                            const float4 ci = *reinterpret_cast<const float4 *>(dst);
-                            o = make_float4(fmaf(alpha, a.x, beta * ci.x), fmaf(alpha, a.y, beta * ci.y),
-                                            fmaf(alpha, a.z, beta * ci.z), fmaf(alpha, a.w, beta * ci.w));
+                            o = make_float4(fmaf(alpha, a.x, beta * ci[i].x), fmaf(alpha, a.y, beta * ci[i].y),
+                                            fmaf(alpha, a.z, beta * ci[i].z), fmaf(alpha, a.w, beta * ci[i].w));
                         } else {
                             o = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
                         }
