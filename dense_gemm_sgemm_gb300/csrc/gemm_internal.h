@@ -45,6 +45,9 @@ struct StreamWorkspace {
 };
 // False when no workspace exists and none can be allocated now (e.g. during capture).
 bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out);
+// Zeroes the arrival counters of every workspace of device `dev` (after a kernel gave up on
+// a bounded wait and may have left counters raised).  Synchronises those streams.
+void reset_workspace_counters(int dev);
 
 // Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
 // A batch of `batch` problems: operand b of problem i starts `stride` elements after that

@@ -21,7 +21,8 @@
 //               while warp 1 already accumulates the next tile into the other buffer.
 //
 // The last, partial wave of tiles is split so that more SMs share it: into K halves whose
-// fp32 partial tiles are added by the half that finishes second, or into N halves.
+// fp32 partial sums are exchanged (each half finishes half of the tile's columns), or into
+// N halves.
 //
 // Tiles are visited in the grouped raster of the copecc "线程块网格重排" section.  Ragged M,
 // N and K need no special code: TMA fills out-of-range elements with zeros, which add
@@ -73,10 +74,11 @@ struct HgemmParams {
     // of the last, partial wave becomes two units, so twice as many SMs share that wave:
     //   tail_mode kTailN: the left and right 128 x 128 halves (every element still summed by
     //     one CTA over all of K, so no result bit changes);
-    //   tail_mode kTailK: the first and second half of the K slices.  Each half stores its
-    //     fp32 partial tile in ws; the half that finishes second (counted in counters) adds
-    //     the other's partial to its own and writes C.  Two fp32 values sum to the same bits
-    //     in either order, so the result does not depend on which half finishes first.
+    //   tail_mode kTailK: the first and second half of the K slices.  Each half stores in ws
+    //     its fp32 partial sums of the other half's 128 columns, waits for the other half's
+    //     arrival (counters), adds the other half's partial to its own columns and writes
+    //     them: every element is the sum of the two K halves' partial sums, the same bits
+    //     whichever half adds.
     // Every K slice costs the ring's round-trip latency whatever the unit's width, so K
     // halves finish the wave in half the time and N halves do not.
     int64_t full_tiles, num_units;
@@ -630,54 +632,73 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     store_chunk(c, v);
                 }
             } else {
-                // K half: publish this half's partial tile, count the arrival; the half that
-                // arrives second adds the other partial and writes C.  Partials are stored
-                // thread-major (float4 q of epilogue thread e at q * 128 + e), so every warp
-                // access is 512 contiguous bytes.  The second half copies the other partial
-                // into the operand ring, idle now (a split unit is its CTA's last unit and
-                // every load into the ring has landed), with 16-byte cp.async.
+                // K half h finishes columns [128 h, 128 h + 128) of the tile.  It publishes
+                // its partial sums of the other half's columns, counts its arrival, waits
+                // (bounded) for the other K half's arrival, copies that half's partial of
+                // its own columns into the operand ring -- idle now: a split unit is its
+                // CTA's last unit and every load into the ring has landed -- with 16-byte
+                // cp.async, adds it and writes C.  Partials are thread-major (float4 q of
+                // epilogue thread e at q * 128 + e), so every warp access is 512 contiguous
+                // bytes.  Both halves belong to this grid, which never exceeds the resident
+                // capacity, so the wait ends unless a fault aborts the kernel.
                 const int e = threadIdx.x - 64;
+                const int h = x.khalf;
                 const int64_t slot = MC ? 2 * x.split_slot + rank : x.split_slot;
-                constexpr int Q = BN / 4;  // float4 per row
-                float4 *mine = reinterpret_cast<float4 *>(p.ws) + (slot * 2 + x.khalf) * (Q * 128) + e;
-                const float4 *other = reinterpret_cast<const float4 *>(p.ws) + (slot * 2 + (x.khalf ^ 1)) * (Q * 128) + e;
+                constexpr int QH = BN / 8;  // float4 per row of a half tile
+                float4 *mine = reinterpret_cast<float4 *>(p.ws) + (slot * 2 + h) * (QH * 128) + e;
+                const float4 *other = reinterpret_cast<const float4 *>(p.ws) + (slot * 2 + (h ^ 1)) * (QH * 128) + e;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int cc = 0; cc < BN / 64; ++cc) {
                     float v[32];
                     __syncwarp();
-                    tmem_ld_32(taddr + c * 32, v);
+                    tmem_ld_32(taddr + ((h ^ 1) * (BN / 64) + cc) * 32, v);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        __stcg(mine + (c * 8 + j) * 128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                        __stcg(mine + (cc * 8 + j) * 128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps' partials
-                bool arrived_second = false;
+                bool failed = false;
                 if (threadIdx.x == 64) {
+                    unsigned int *ctr = p.counters + slot;
                     __threadfence();  // release this CTA's partial (cumulative over the barrier)
-                    arrived_second = atomicAdd(p.counters + slot, 1u) == 1u;
-                    if (arrived_second) {
-                        p.counters[slot] = 0;  // ready for the next launch
-                        __threadfence();       // acquire the other half's partial
+                    atomicAdd(ctr, 1u);
+                    const uint64_t t0 = global_timer_ns();
+                    for (uint32_t it = 0;; ++it) {
+                        uint32_t seen;
+                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+                        if (seen >= 2u) break;
+                        if ((it & 15u) == 0 && (*abort_flag || global_timer_ns() - t0 > tmo)) {
+                            failed = true;
+                            break;
+                        }
+                    }
+                    if (!failed) {
+                        __threadfence();  // acquire the other half's partial for the whole CTA
+                        // both halves have seen both arrivals: the second to get here resets
+                        if (atomicAdd(ctr, 1u) == 3u) *ctr = 0u;
                     }
                 }
-                if (epilogue_any(arrived_second)) {
-                    static_assert(Q * 128 * 16 <= STAGES * STAGE_BYTES, "the ring holds a partial tile");
+                if (epilogue_any(failed)) {
+                    raise_abort(abort_flag);
+                } else {
+                    static_assert(QH * 128 * 16 <= STAGES * STAGE_BYTES, "the ring holds a partial half tile");
                     const uint32_t stage_dst = sA + uint32_t(e) * 16u;
 #pragma unroll 8
-                    for (int q = 0; q < Q; ++q)
+                    for (int q = 0; q < QH; ++q)
                         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stage_dst + uint32_t(q) * 2048u),
                                      "l"(other + q * 128)
                                      : "memory");
                     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
                     const float4 *staged = reinterpret_cast<const float4 *>(smem) + e;
 #pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int cc = 0; cc < BN / 64; ++cc) {
+                        const int c = h * (BN / 64) + cc;
                         float v[32];
                         __syncwarp();
                         tmem_ld_32(taddr + c * 32, v);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const float4 o = staged[(c * 8 + j) * 128];
+                            const float4 o = staged[(cc * 8 + j) * 128];
                             v[4 * j] += o.x; v[4 * j + 1] += o.y; v[4 * j + 2] += o.z; v[4 * j + 3] += o.w;
                         }
                         store_chunk(c, v);
@@ -909,7 +930,12 @@ gemm_status_t read_and_clear_device_status(cudaStream_t stream)
     if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof(word)) != cudaSuccess ||
         cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
-    return word ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+    if (word) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) reset_workspace_counters(dev);
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
 }
 
 }  // namespace gemm

@@ -4,7 +4,8 @@
 // calls on different streams never do.  It is allocated once, on the first call on that
 // stream that splits K, kept until the process exits, and never allocated while the stream
 // is being captured (the call then runs without splitting).  Every kernel that uses the
-// arrival counters leaves them at zero when it finishes.
+// arrival counters leaves them at zero when it finishes -- unless it gave up on a bounded
+// wait, after which reset_workspace_counters() restores them.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -44,6 +45,17 @@ bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out)
     g_ws[{dev, stream}] = w;
     out = w;
     return true;
+}
+
+void reset_workspace_counters(int dev)
+{
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto &kv : g_ws)
+        if (kv.first.first == dev) {
+            cudaStreamSynchronize(kv.first.second);
+            cudaMemset(kv.second.counters, 0, kWorkspaceCounters * sizeof(unsigned int));
+        }
+    cudaGetLastError();
 }
 
 }  // namespace gemm

@@ -171,7 +171,10 @@ GEMM_API gemm_status_t gemm_sgemm_f32_noalloc(gemm_op_t opA, gemm_op_t opB, int6
 /*
  * Waits for `stream`, then returns and clears the error word that kernels of this library
  * set on the current device when a bounded barrier wait expires (GEMM_ERR_DEVICE_TIMEOUT),
- * or GEMM_OK.  A kernel that sets the word leaves its output tile unwritten.
+ * or GEMM_OK.  A kernel that sets the word leaves its output tile unwritten.  After a
+ * timeout it also synchronises every stream of the current device that owns a split-K
+ * workspace and zeroes that workspace's arrival counters, which an abandoned wait may have
+ * left raised.
  */
 GEMM_API gemm_status_t gemm_get_device_status(void *stream);
 
