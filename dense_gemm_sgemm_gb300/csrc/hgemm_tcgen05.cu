@@ -69,7 +69,8 @@ struct HgemmParams {
     int num_kb;
     int c_vec;               // C base 16-byte aligned and ldc % 4 == 0
     uint64_t timeout_ns;     // limit of every barrier wait
-    int inject_stall;        // test hook: the producer never fills the first slice
+    int inject_stall;        // test hook: 1 = the producer never fills the first slice of its
+                             // first unit; 2 = nor of a first K half of the tail
     // Work units.  Units [0, full_tiles) are whole 128 x 256 tiles over all of K.  Each tile
     // of the last, partial wave becomes two units, so twice as many SMs share that wave:
     //   tail_mode kTailN: the left and right 128 x 128 halves (every element still summed by
@@ -435,7 +436,8 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     mbar_expect_tx(fb, bytes);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    const bool stall = p.inject_stall && u == unit0 && kb == x.kb0;
+                    const bool stall = kb == x.kb0 && ((p.inject_stall == 1 && u == unit0) ||
+                                                       (p.inject_stall == 2 && x.khalf == 0));
                     if (!stall) {
                         const int32_t k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
@@ -912,8 +914,8 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     p.ab_format = bf ? 1u : 0u;
     p.timeout_ns = 2000000000ull;
     p.inject_stall = 0;
-    if (const char *e = std::getenv("GEMM_GB300_TEST_INJECT_STALL"); e && e[0] == '1') {
-        p.inject_stall = 1;
+    if (const char *e = std::getenv("GEMM_GB300_TEST_INJECT_STALL"); e && (e[0] == '1' || e[0] == '2')) {
+        p.inject_stall = e[0] - '0';
         p.timeout_ns = 20000000ull;
     }
     cudaError_t e;
