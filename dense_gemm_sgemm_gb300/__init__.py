@@ -171,7 +171,8 @@ def matmul(A, B, C=None, alpha=1.0, beta=0.0, opA="N", opB="N", stream=None):
 
     A and B are 2-D CUDA tensors holding the STORED matrices (row stride = leading
     dimension, unit column stride); fp32 operands go to gemm_sgemm_f32, fp16 operands to
-    gemm_hgemm_f16f32.  C (fp32, M x N) is created when omitted (then beta must be 0).
+    gemm_hgemm_f16f32, bf16 operands to gemm_bgemm_bf16f32.  C (fp32, M x N) is created
+    when omitted (then beta must be 0).
     """
     import torch
 
