@@ -38,7 +38,8 @@ constexpr size_t kWsCounters = kWorkspaceCounters;
 // 256^2 to 3072^2, K = 128 / 513 / 1024 / 4096, op(A) = N and T, every configuration and split
 // count below; the rule picks a plan within 1.6% of the fastest measured one on average).
 struct CfgDesc {
-    char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
+    char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4),
+                // 'X' = 128 x 256 (8 x 16, one CTA per SM)
     int bm, bn, min_blocks;
     bool a_k_major;  // a K-contiguous A is staged [x][k] (else transposed to [k][x])
     int max_splits;
@@ -63,6 +64,7 @@ const CfgDesc kCfgs[] = {
     desc<CfgL>('L', 4, 1.442, 3.156, 1.764, launch_L, launch_LS),
     desc<CfgM>('M', 12, 0.857, 1.723, 0.464, launch_M, launch_MS),
     desc<CfgS>('S', 16, 0.471, 1.429, 0.015, launch_S, launch_SS),
+    desc<CfgX>('X', 1, 1e9, 0.0, 0.0, launch_X, launch_X),  // outside the model: see choose_plan
 };
 
 const CfgDesc *find_cfg(char name)
@@ -83,6 +85,10 @@ struct Plan {
 // (slices per CTA) * (CTAs on the busiest SM) * us_slice + us_fixed, and every split adds
 // us_split.  Splits come from {1, 2, 3, 4, 6, 8, 12, 16} (at most max_splits, at least two
 // K slices each) and cost 2% extra in the comparison, so near ties keep K whole.
+// The 128 x 256 tile (one CTA per SM) has the best steady state but a large cost per wave
+// that its CTAs cannot hide behind a co-resident CTA; it is taken, unsplit, only for grids of
+// at least 8 waves that fill 94% of their last wave, with K >= 1024 (measured: 16384^2 x 1024
+// 8660 -> 8410 us; at 4096^3, 3.4 waves, it is 11% slower than the 128 x 128 tile).
 // Split-K needs the workspace: at most kWsCounters tiles and kWsBytes of partial tiles.
 // GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps.
 Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool allow_split)
@@ -109,6 +115,7 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
     double best = -1.0;
     for (const CfgDesc &c : kCfgs)
         for (int S : kSplits) {
+            if (c.name == 'X') continue;
             if (!fits(c, S) || (S > 1 && KT / S < 2)) continue;
             const double t = cost(c, S);
             if (best < 0.0 || t < best) {
@@ -116,6 +123,11 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
                 plan = {&c, S};
             }
         }
+    const CfgDesc &X = *find_cfg('X');
+    const int64_t tiles_x = tiles(X);
+    const int64_t waves_x = (tiles_x + num_sms - 1) / num_sms;
+    if (K >= 1024 && tiles_x >= 8 * int64_t(num_sms) && double(tiles_x) >= 0.94 * double(waves_x * num_sms))
+        plan = {&X, 1};
     if (const char *e = std::getenv("GEMM_GB300_SGEMM_PLAN")) {
         const CfgDesc *c = find_cfg(e[0]);
         if (c != nullptr && e[1] == ':') {

@@ -140,19 +140,31 @@ struct SliceLoader<kMnVec, W, BK> {
     static constexpr int CPR = W / 4;              // 16-byte chunks per k row
     static constexpr int R = BK * CPR / kThreads;  // copies per thread
     static constexpr int KSTEP = kThreads / CPR;   // k distance between a thread's copies
-    static_assert(BK * CPR % kThreads == 0 && KSTEP % 8 == 0, "");
+    static_assert(BK * CPR % kThreads == 0 && (KSTEP % 8 == 0 || 8 % KSTEP == 0), "");
     const float *p;   // element (kb, x) of slice 0
     int kb;           // first k row of this thread
+    int c;            // 16-byte chunk of this thread within a k row
     uint32_t bytes;   // valid bytes of this thread's chunk (ragged x tail)
     uint32_t dst0;    // byte offset in a stage
     __device__ __forceinline__ SliceLoader(const float *X, int64_t ld, int64_t ext, int64_t x0, int tid)
     {
-        const int c = tid % CPR;
+        c = tid % CPR;
         kb = tid / CPR;
         const int64_t rem = ext - (x0 + 4 * c);
         bytes = rem <= 0 ? 0u : (rem >= 4 ? 16u : static_cast<uint32_t>(rem * 4));
         p = X + kb * ld + (bytes ? x0 + 4 * c : 0);
         dst0 = static_cast<uint32_t>(kb * W + ((c ^ (kb & 7)) << 2)) * 4u;
+    }
+    // Byte offset of copy r: rows KSTEP apart keep the swizzle of row kb when KSTEP is a
+    // multiple of 8; otherwise each row takes its own.
+    __device__ __forceinline__ uint32_t dst(int r) const
+    {
+        if constexpr (KSTEP % 8 == 0) {
+            return dst0 + r * KSTEP * W * 4;
+        } else {
+            const int k = kb + r * KSTEP;
+            return static_cast<uint32_t>(k * W + ((c ^ (k & 7)) << 2)) * 4u;
+        }
     }
     __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
                                          int64_t K) const
@@ -161,7 +173,7 @@ struct SliceLoader<kMnVec, W, BK> {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const bool ok = bytes && (k0 + kb + r * KSTEP < K);
-            cp_async16(stage + dst0 + r * KSTEP * W * 4, ok ? q + r * KSTEP * ld : base, ok ? bytes : 0u);
+            cp_async16(stage + dst(r), ok ? q + r * KSTEP * ld : base, ok ? bytes : 0u);
         }
     }
 };
@@ -731,7 +743,8 @@ cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, 
 using CfgL = Cfg<128, 128, 16, 8, 8, 4, 2>;  // 8 x 8 per thread, two CTAs per SM
 using CfgM = Cfg<128, 64, 16, 8, 4, 4, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
 using CfgS = Cfg<64, 64, 16, 4, 4, 4, 3>;    // 4 x 4 per thread, three CTAs per SM
-static_assert(CfgL::BK == 16 && CfgM::BK == 16 && CfgS::BK == 16,
+using CfgX = Cfg<128, 256, 16, 8, 16, 4, 1>; // 8 x 16 per thread, one CTA per SM
+static_assert(CfgL::BK == 16 && CfgM::BK == 16 && CfgS::BK == 16 && CfgX::BK == 16,
               "the host planner counts K in slices of 16");
 
 // Launchers defined in the configuration translation units.
@@ -739,6 +752,7 @@ cudaError_t launch_L(int dev_id, int a_mode, int b_mode, const SgemmParams &p, c
 cudaError_t launch_LS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_M(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_MS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_X(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_S(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_SS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 
