@@ -74,10 +74,12 @@ const CfgDesc *find_cfg(char name)
     return nullptr;
 }
 
-// A launch plan: tile configuration and K splits.
+// A launch plan: tile configuration, K splits, and the number of leading tiles that run
+// whole (0: every tile is split; see SgemmParams::full_tiles).
 struct Plan {
     const CfgDesc *cfg;
     int splits;
+    int64_t full_tiles;
 };
 
 // Plan rule: the (configuration, splits) pair of least modelled time.  CTAs run in waves of
@@ -90,7 +92,8 @@ struct Plan {
 // at least 8 waves that fill 94% of their last wave, with K >= 1024 (measured: 16384^2 x 1024
 // 8660 -> 8410 us; at 4096^3, 3.4 waves, it is 11% slower than the 128 x 128 tile).
 // Split-K needs the workspace: at most kWsCounters tiles and kWsBytes of partial tiles.
-// GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps.
+// GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps; an
+// unsplit override still gets the last-wave split below unless GEMM_GB300_SGEMM_TAIL=0.
 Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool allow_split)
 {
     // a batch multiplies the tiles (and the split-K partials) of one problem
@@ -111,7 +114,7 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
         return t;
     };
     static const int kSplits[] = {1, 2, 3, 4, 6, 8, 12, 16};
-    Plan plan{find_cfg('L'), 1};
+    Plan plan{find_cfg('L'), 1, 0};
     double best = -1.0;
     for (const CfgDesc &c : kCfgs)
         for (int S : kSplits) {
@@ -120,19 +123,44 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
             const double t = cost(c, S);
             if (best < 0.0 || t < best) {
                 best = t;
-                plan = {&c, S};
+                plan = {&c, S, 0};
             }
         }
     const CfgDesc &X = *find_cfg('X');
     const int64_t tiles_x = tiles(X);
     const int64_t waves_x = (tiles_x + num_sms - 1) / num_sms;
     if (K >= 1024 && tiles_x >= 8 * int64_t(num_sms) && double(tiles_x) >= 0.94 * double(waves_x * num_sms))
-        plan = {&X, 1};
+        plan = {&X, 1, 0};
     if (const char *e = std::getenv("GEMM_GB300_SGEMM_PLAN")) {
         const CfgDesc *c = find_cfg(e[0]);
         if (c != nullptr && e[1] == ':') {
             const int f = std::atoi(e + 2);
-            if (f >= 1 && fits(*c, f)) plan = {c, f};
+            if (f >= 1 && fits(*c, f)) plan = {c, f, 0};
+        }
+    }
+    // Last partial wave of the 128 x 128 tile (two CTAs per SM).  A CTA alone on its SM runs
+    // about twice as fast as one sharing it, so a last wave of tail <= num_sms tiles already
+    // takes ~1/2 of a full wave.  Split S ways, it takes ~1/(2S) when S * tail <= num_sms
+    // (each split still alone) or ~1/S when S * tail fits two per SM.  The split is taken when
+    // it reaches 0.4 or less (4096^3: 112 tail tiles, no split pays; 5120^2 x 2048: 80 tail
+    // tiles in 3 splits, 1762 -> 1736 us).  At least 4 K slices per split.
+    const char *tail_env = std::getenv("GEMM_GB300_SGEMM_TAIL");  // "0": never split the last wave
+    if (plan.splits == 1 && batch == 1 && allow_split && plan.cfg->name == 'L' &&
+        !(tail_env && tail_env[0] == '0')) {
+        const CfgDesc &c = *plan.cfg;
+        const int64_t t = tiles(c), slots = int64_t(num_sms) * c.min_blocks, tail = t % slots;
+        if (t >= slots && tail > 0 && tail <= int64_t(num_sms) && tail <= int64_t(kWsCounters)) {
+            double best_rel = 0.4;
+            int best_s = 0;
+            for (int S = 2; S <= c.max_splits; ++S) {
+                if (KT / S < 4 || size_t(tail) * S * c.bm * c.bn * 4 > kWsBytes) continue;
+                const double rel = tail * S <= num_sms ? 1.0 / (2 * S) : (tail * S <= slots ? 1.0 / S : 1.0);
+                if (rel <= best_rel) {
+                    best_rel = rel;
+                    best_s = S;
+                }
+            }
+            if (best_s > 0) plan = {&c, best_s, t - tail};
         }
     }
     return plan;
@@ -159,7 +187,8 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     // element of the operand: relative to the GEMM's 2 M N K flops that is 1-2% when the
     // other output dimension is 2048 or more, and its launch is negligible above 1e10 flops.
     // Without scratch the transposing copies remain.
-    if (!cfg.a_k_major && plan.splits == 1 && 2.0 * double(M) * double(N) * double(K) * double(batch) >= 1e10) {
+    if (!cfg.a_k_major && (plan.splits == 1 || plan.full_tiles > 0) &&
+        2.0 * double(M) * double(N) * double(K) * double(batch) >= 1e10) {
         const int64_t kOther = 2048;
         const float *t = nullptr;
         int64_t ldt = 0, st = 0;
@@ -198,10 +227,20 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     p.tiles_m = (M + cfg.bm - 1) / cfg.bm;
     p.tiles_n = (N + cfg.bn - 1) / cfg.bn;
     p.splits = plan.splits;
+    p.full_tiles = plan.full_tiles;
     p.kt_per_split = (KT + plan.splits - 1) / plan.splits;
     if (plan.splits > 1) {
         p.ws = w.data;
         p.counters = w.counters;
+        if (plan.full_tiles > 0) {
+            // The whole tiles run in the kernel without split-K code (the split variant needs
+            // more registers and would slow every tile), then the split last wave.
+            SgemmParams pw = p;
+            pw.splits = 1;
+            const cudaError_t e = cfg.launch(dev.device, a_mode, b_mode, pw, stream);
+            if (e != cudaSuccess) return e;
+            p.cta_offset = plan.full_tiles;
+        }
         return cfg.launch_split(dev.device, a_mode, b_mode, p, stream);
     }
     return cfg.launch(dev.device, a_mode, b_mode, p, stream);

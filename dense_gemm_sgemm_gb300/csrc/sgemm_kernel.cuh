@@ -56,7 +56,14 @@ struct SgemmParams {
     int64_t tiles_m, tiles_n;
     int log_group;
     int c_vec;  // C base 16-byte aligned and ldc % 4 == 0
-    // Split-K (gridDim.y = splits): split s sums k slices [s*kt_per_split, (s+1)*kt_per_split).
+    // Split-K: tiles [0, full_tiles) of a problem run whole, one CTA each; every later tile
+    // runs as `splits` CTAs, split s summing k slices [s*kt_per_split, (s+1)*kt_per_split).
+    // CTA b of a problem (blockIdx.x) takes tile b when b < full_tiles, else tile
+    // full_tiles + (b - full_tiles) / splits, split (b - full_tiles) % splits.  full_tiles = 0
+    // splits every tile; a positive full_tiles splits only the last, partial wave, and the
+    // host then launches the whole tiles (without split-K code) and the split ones apart:
+    // a launch covers CTAs [cta_offset, cta_offset + gridDim.x).
+    int64_t full_tiles, cta_offset;
     int splits, kt_per_split;
     float *ws;               // splits x tiles partial tiles (splits > 1 only)
     unsigned int *counters;  // one arrival counter per tile, zero between launches
@@ -415,7 +422,7 @@ struct Acc {
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
                                            const float *__restrict__ B, float *__restrict__ Cmat,
-                                           int64_t tile_id);
+                                           int64_t tile, int split, int nsplit, int64_t slot);
 
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(const SgemmParams p)
@@ -423,15 +430,26 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
     // One problem per CTA: problem blockIdx.z of this launch (the host launches batches of
     // more than 65535 problems in chunks).
     const int64_t z = blockIdx.z;
+    const int64_t b = blockIdx.x + p.cta_offset;
+    int64_t tile = b, slot = 0;
+    int split = 0, nsplit = 1;
+    if (SPLIT && b >= p.full_tiles) {
+        const int64_t r = b - p.full_tiles;
+        tile = p.full_tiles + r / p.splits;
+        split = static_cast<int>(r % p.splits);
+        nsplit = p.splits;
+        slot = z * (p.tiles_m * p.tiles_n - p.full_tiles) + (tile - p.full_tiles);
+    }
     sgemm_tile<C, A_MODE, B_MODE, SPLIT>(p, p.A + z * p.stride_a, p.B + z * p.stride_b, p.C + z * p.stride_c,
-                                         z * (p.tiles_m * p.tiles_n) + blockIdx.x);
+                                         tile, split, nsplit, slot);
 }
 
-// One output tile of one problem.  tile_id numbers the split-K partials and counters.
+// One output tile (or one K split of it) of one problem.  slot numbers the split tile's
+// partials and arrival counter among all split tiles of the launch.
 template <class C, int A_MODE, int B_MODE, bool SPLIT>
 __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
                                            const float *__restrict__ B, float *__restrict__ Cmat,
-                                           int64_t tile_id)
+                                           int64_t tile, int split, int nsplit, int64_t slot)
 {
     extern __shared__ __align__(16) float smem[];
     float *sA = smem;
@@ -443,12 +461,11 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     const int tx = (warp % (C::TX / 8)) * 8 + (lane & 7);
 
     int64_t tm, tn;
-    raster(blockIdx.x, p.tiles_m, p.tiles_n, p.log_group, tm, tn);
+    raster(tile, p.tiles_m, p.tiles_n, p.log_group, tm, tn);
     const int64_t m0 = tm * C::BM, n0 = tn * C::BN;
     const int KT_all = static_cast<int>((p.K + C::BK - 1) / C::BK);
-    const int split = SPLIT ? static_cast<int>(blockIdx.y) : 0;
-    const int kt0 = SPLIT ? split * p.kt_per_split : 0;
-    const int KT = SPLIT ? min(KT_all - kt0, p.kt_per_split) : KT_all;  // slices of this CTA
+    const int kt0 = split * p.kt_per_split;
+    const int KT = nsplit > 1 ? min(KT_all - kt0, p.kt_per_split) : KT_all;  // slices of this CTA
 
     const uint32_t sA_addr = smem_addr(sA), sB_addr = smem_addr(sB);
     const SliceLoader<A_MODE, C::BM, C::BK> la(A, p.lda, p.M, m0, tid);
@@ -469,7 +486,7 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 
     // The epilogue reads C when beta != 0: ask L2 for this thread's rows now, so the reads
     // at the end do not wait for DRAM.
-    if (p.beta != 0.0f && (!SPLIT || split == 0)) {
+    if (p.beta != 0.0f && split == 0) {
 #pragma unroll
         for (int i = 0; i < C::TM; ++i) {
             const int64_t gm = m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4);
@@ -522,15 +539,14 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     }
     cp_async_wait<0>();
 
-    if constexpr (SPLIT) {
+    if (SPLIT && nsplit > 1) {
         // Deterministic split-K: every split stores its partial tile, and the split that
         // arrives last adds all partials in split order 0, 1, ..., splits-1 -- the same
         // order whichever CTA finishes last -- before the epilogue.
         constexpr int Q = C::TM * C::TN / 4;  // float4 per thread
         constexpr int QR = C::TN / 4;         // float4 per accumulator row
-        const int64_t tile = tile_id;
         const int64_t tile4 = int64_t(C::BM) * C::BN / 4;
-        float4 *all = reinterpret_cast<float4 *>(p.ws) + tile * p.splits * tile4;
+        float4 *all = reinterpret_cast<float4 *>(p.ws) + slot * nsplit * tile4;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             const int i = q / QR, j = 4 * (q % QR);
@@ -541,9 +557,9 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         __shared__ unsigned int s_last;
         __syncthreads();
         if (tid == 0) {
-            const unsigned int prev = atomicAdd(p.counters + tile, 1u);
-            s_last = prev == static_cast<unsigned int>(p.splits - 1);
-            if (s_last) p.counters[tile] = 0;  // ready for the next launch
+            const unsigned int prev = atomicAdd(p.counters + slot, 1u);
+            s_last = prev == static_cast<unsigned int>(nsplit - 1);
+            if (s_last) p.counters[slot] = 0;  // ready for the next launch
         }
         __syncthreads();
         const bool last = s_last != 0;
@@ -551,7 +567,7 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         if (!last) return;
         __threadfence();
         // One round per split, Q independent loads in flight per round.
-        for (int s2 = 0; s2 < p.splits; ++s2) {
+        for (int s2 = 0; s2 < nsplit; ++s2) {
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const float4 u = __ldcg(all + s2 * tile4 + q * kThreads + tid);
@@ -671,7 +687,9 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
         attr_set.fetch_or(bit, std::memory_order_release);
     }
     const int64_t tiles = p.tiles_m * p.tiles_n;
-    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const int64_t ctas = SPLIT ? p.full_tiles + (tiles - p.full_tiles) * p.splits - p.cta_offset
+                               : (p.full_tiles > 0 ? p.full_tiles : tiles);
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     // gridDim.z holds at most 65535 problems: larger batches go in consecutive launches on the
     // same stream (which also keeps their split-K workspace use in order).
     constexpr int64_t kMaxZ = 65535;
@@ -681,7 +699,7 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
         q.A = p.A + b0 * p.stride_a;
         q.B = p.B + b0 * p.stride_b;
         q.C = p.C + b0 * p.stride_c;
-        const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits), static_cast<unsigned>(q.batch));
+        const dim3 grid(static_cast<unsigned>(ctas), 1u, static_cast<unsigned>(q.batch));
         kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(q);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -103,6 +103,31 @@ def test_every_tile_configuration(plan, monkeypatch):
         parity.check_full(wi, inputs, dev["C"], integer=True)
 
 
+# An unsplit 128 x 128 plan whose last wave is small runs that wave's tiles as K splits in a
+# second launch (fixed-order sum by the last split); GEMM_GB300_SGEMM_TAIL=0 turns that off.
+# 2304^2: 324 tiles of 128 x 128 (one wave of 304 + 20 -> 4 splits); the 128 x 64 and 64 x 64
+# plans run unsplit (covered here as the reference behaviour).
+@pytest.mark.parametrize("plan", ["L:1", "M:1", "S:1"])
+@pytest.mark.parametrize("opA,opB", [("N", "N"), ("T", "T")])
+def test_last_wave_split(plan, opA, opB, monkeypatch):
+    monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", plan)
+    wi = workloads.Workload(f"tail_int_{plan}_{opA}{opB}", "f32", 2304, 2304, 300, opA, opB,
+                            seed=41, dist_a="int4", dist_b="int4", pad=(1, 0, 0))
+    inputs, dev = _run(wi)
+    parity.check_full(wi, inputs, dev["C"], integer=True)
+    w = workloads.Workload(f"tail_{plan}_{opA}{opB}", "f32", 2304, 2300, 300, opA, opB,
+                           alpha=0.5, beta=-1.5, seed=42)
+    inputs, dev = _run(w)
+    split = dev["C"].clone()
+    parity.check_full(w, inputs, split)
+    monkeypatch.setenv("GEMM_GB300_SGEMM_TAIL", "0")
+    dev["C"].copy_(inputs["C"].cuda())
+    parity.run_library(w, dev)
+    torch.cuda.synchronize()
+    assert gemm_get_device_status() == 0
+    parity.check_full(w, inputs, dev["C"])
+
+
 # Large problems on the 128-row tiles transpose a K-contiguous operand into scratch first
 # (op(A) = N when N >= 2048, op(B) = T when M >= 2048, at 1e10 flops or more): unaligned
 # leading dimensions, ragged K and both operands at once.
