@@ -22,6 +22,7 @@ __all__ = [
     "gemm_bgemm_bf16f32", "gemm_sgemm_f32_strided_batched", "gemm_hgemm_f16f32_strided_batched",
     "gemm_bgemm_bf16f32_strided_batched", "gemm_sgemm_f32_noalloc",
     "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
+    "gemm_kernel_launches",
     "library_path", "load", "matmul",
 ]
 
@@ -155,6 +156,11 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_version() -> int:
     return int(load().gemm_version())
+
+
+def gemm_kernel_launches() -> int:
+    """Kernels this process has launched through the library so far (for accounting)."""
+    return int(load().gemm_kernel_launches())
 
 
 def gemm_tile_raster(t, tiles_m, tiles_n, log_group):

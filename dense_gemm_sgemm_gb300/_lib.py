@@ -40,6 +40,7 @@ SIGNATURES = {
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_status_string": (ctypes.c_char_p, [_int]),
     "gemm_version": (_int, []),
+    "gemm_kernel_launches": (ctypes.c_uint64, []),
     "gemm_tile_raster": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64),
                                 ctypes.POINTER(_i64)]),
 }

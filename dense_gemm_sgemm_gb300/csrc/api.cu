@@ -233,6 +233,8 @@ const char *gemm_status_string(gemm_status_t status)
 
 int gemm_version(void) { return 100; }
 
+uint64_t gemm_kernel_launches(void) { return gemm::launches_so_far(); }
+
 gemm_status_t gemm_tile_raster(int64_t t, int64_t tiles_m, int64_t tiles_n, int log_group,
                                int64_t *tile_m, int64_t *tile_n)
 {

@@ -92,6 +92,10 @@ bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float 
 cudaError_t launch_scale_batched(int64_t M, int64_t N, float beta, float *C, int64_t ldc,
                                  int64_t strideC, int64_t batch, cudaStream_t stream);
 
+// Counts kernel launches of the library (gemm_kernel_launches).
+void count_launches(uint64_t n = 1);
+uint64_t launches_so_far();
+
 // Reads and clears the device error word (synchronises `stream`).
 gemm_status_t read_and_clear_device_status(cudaStream_t stream);
 

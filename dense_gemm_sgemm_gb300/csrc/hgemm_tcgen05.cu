@@ -855,7 +855,9 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         if (e != cudaSuccess) return e;
         hgemm_tcgen05_kernel<A_MN, B_MN, false><<<static_cast<unsigned>(workers), kThreads, SMEM_BYTES, stream>>>(
             m.a, m.b, m.b_half, m.b_quarter, p);
-        return cudaGetLastError();
+        const cudaError_t le = cudaGetLastError();
+        if (le == cudaSuccess) count_launches();
+        return le;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * workers), 1, 1);
@@ -869,7 +871,10 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true>, m.a, m.b, m.b_half, m.b_quarter, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true>, m.a, m.b, m.b_half,
+                                             m.b_quarter, p);
+    if (e == cudaSuccess) count_launches();
+    return e;
 }
 
 }  // namespace

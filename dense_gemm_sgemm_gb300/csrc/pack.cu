@@ -133,6 +133,7 @@ bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float 
         transpose_f32<<<grid, 256, 0, stream>>>(src + b0 * stride, ld, stride, dst + b0 * cols * ldt, ldt,
                                                         cols * ldt, rows, cols);
         if (cudaGetLastError() != cudaSuccess) return false;
+        count_launches();
     }
     *out = dst;
     *ld_out = ldt;
@@ -155,6 +156,7 @@ bool pack_u16_operand(int dev, cudaStream_t stream, int which, const uint16_t *s
     if (blocks < 1) blocks = 1;
     pack_rows_u16<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld, stride, dst, ldp, rows, cols, nb);
     if (cudaGetLastError() != cudaSuccess) return false;
+    count_launches();
     *out = dst;
     *ld_out = ldp;
     *stride_out = stride == 0 ? 0 : rows * ldp;

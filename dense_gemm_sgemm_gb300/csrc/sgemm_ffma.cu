@@ -263,7 +263,9 @@ cudaError_t launch_scale(int64_t M, int64_t N, float beta, float *C, int64_t ldc
     int64_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, beta, C, ldc);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches();
+    return e;
 }
 
 }  // namespace gemm

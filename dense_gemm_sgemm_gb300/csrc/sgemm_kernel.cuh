@@ -703,6 +703,7 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
         kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(q);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        count_launches();
     }
     return cudaSuccess;
 }

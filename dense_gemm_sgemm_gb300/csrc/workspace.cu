@@ -1,4 +1,5 @@
-// Per-(device, stream) workspace of the split-K paths of both kernels.
+// Per-(device, stream) workspace of the split-K paths of both kernels, and the library's
+// kernel-launch counter.
 //
 // One workspace per (device, stream): calls on the same stream are ordered and may share it;
 // calls on different streams never do.  It is allocated once, on the first call on that
@@ -8,6 +9,7 @@
 // wait, after which reset_workspace_counters() restores them.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -16,6 +18,7 @@
 
 namespace gemm {
 namespace {
+std::atomic<uint64_t> g_launches{0};
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, StreamWorkspace> g_ws;
 }  // namespace
@@ -46,6 +49,10 @@ bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out)
     out = w;
     return true;
 }
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 
 void reset_workspace_counters(int dev)
 {

@@ -185,6 +185,13 @@ GEMM_API const char *gemm_status_string(gemm_status_t status);
 GEMM_API int gemm_version(void);
 
 /*
+ * Number of kernels this process has launched through the library so far, on every device
+ * and stream (GEMM kernels and the operand re-layout and scaling kernels).  For accounting:
+ * the difference across a region counts the library's launches in it.  Needs no GPU.
+ */
+GEMM_API uint64_t gemm_kernel_launches(void);
+
+/*
  * Tile raster used by the kernels (a host function: needs no GPU).  It maps the t-th tile
  * of a tiles_m x tiles_n grid of output tiles to (tile_m, tile_n) so that consecutive
  * tiles sweep a group of 2^log_group tile rows column by column, which keeps the operand
