@@ -539,6 +539,41 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     }
     cp_async_wait<0>();
 
+    // Small-tile split kernels read their C values (beta != 0) before the split-K hand-off,
+    // so the split that arrives last does not wait for them after it (C is written only by
+    // that split).
+    const float alpha = p.alpha, beta = p.beta;
+    auto row_of = [&](int i) { return m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4); };
+    auto col_of = [&](int jb) { return n0 + jb * C::N_STRIDE + tx * 4; };
+    constexpr bool kSmallTile = C::TM * C::TN <= 16;
+    float4 cin[kSmallTile ? C::TM : 1][kSmallTile ? C::NB : 1];
+    auto read_c = [&]() {
+#pragma unroll
+        for (int i = 0; i < C::TM; ++i) {
+            const int64_t gm = row_of(i);
+            const float *crow = Cmat + (gm < p.M ? gm * p.ldc : 0);
+#pragma unroll
+            for (int jb = 0; jb < C::NB; ++jb) {
+                const int64_t gn = col_of(jb);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gm < p.M) {
+                    if (p.c_vec && gn + 3 < p.N) {
+                        v = *reinterpret_cast<const float4 *>(crow + gn);
+                    } else {
+                        v.x = gn + 0 < p.N ? crow[gn + 0] : 0.0f;
+                        v.y = gn + 1 < p.N ? crow[gn + 1] : 0.0f;
+                        v.z = gn + 2 < p.N ? crow[gn + 2] : 0.0f;
+                        v.w = gn + 3 < p.N ? crow[gn + 3] : 0.0f;
+                    }
+                }
+                cin[i][jb] = v;
+            }
+        }
+    };
+    if constexpr (kSmallTile) {
+        if (beta != 0.0f) read_c();
+    }
+
     if (SPLIT && nsplit > 1) {
         // Deterministic split-K: every split stores its partial tile, and the split that
         // arrives last adds all partials in split order 0, 1, ..., splits-1 -- the same
@@ -582,10 +617,7 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     }
 
     // Epilogue: C = alpha * acc + beta * C, beta == 0 never reads C.
-    const float alpha = p.alpha, beta = p.beta;
-    auto row_of = [&](int i) { return m0 + (i / 4) * C::M_STRIDE + ty * 4 + (i % 4); };
-    auto col_of = [&](int jb) { return n0 + jb * C::N_STRIDE + tx * 4; };
-    if constexpr (C::TM * C::TN > 16) {
+    if constexpr (!kSmallTile) {
         // Large thread tiles (long-running CTAs): one pass, read-modify-write per 4-vector.
 #pragma unroll
         for (int i = 0; i < C::TM; ++i) {
@@ -618,32 +650,19 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         return;
     }
     // Small thread tiles (short-lived CTAs, where the epilogue is a large share of the time):
-    // two passes, first every read of C (loads only, so they are all in flight together),
-    // then every store.
+    // every read of C was issued above, all in flight together; then every store.
     if (beta != 0.0f) {
 #pragma unroll
         for (int i = 0; i < C::TM; ++i) {
-            const int64_t gm = row_of(i);
-            if (gm >= p.M) continue;
-            const float *crow = Cmat + gm * p.ldc;
 #pragma unroll
             for (int jb = 0; jb < C::NB; ++jb) {
-                const int64_t gn = col_of(jb);
-                float4 cin;
-                if (p.c_vec && gn + 3 < p.N) {
-                    cin = *reinterpret_cast<const float4 *>(crow + gn);
-                } else {
-                    cin.x = gn + 0 < p.N ? crow[gn + 0] : 0.0f;
-                    cin.y = gn + 1 < p.N ? crow[gn + 1] : 0.0f;
-                    cin.z = gn + 2 < p.N ? crow[gn + 2] : 0.0f;
-                    cin.w = gn + 3 < p.N ? crow[gn + 3] : 0.0f;
-                }
+                const float4 c4 = cin[i][jb];
                 float &v0 = acc.at(i, 4 * jb), &v1 = acc.at(i, 4 * jb + 1);
                 float &v2 = acc.at(i, 4 * jb + 2), &v3 = acc.at(i, 4 * jb + 3);
-                v0 = fmaf(alpha, v0, beta * cin.x);
-                v1 = fmaf(alpha, v1, beta * cin.y);
-                v2 = fmaf(alpha, v2, beta * cin.z);
-                v3 = fmaf(alpha, v3, beta * cin.w);
+                v0 = fmaf(alpha, v0, beta * c4.x);
+                v1 = fmaf(alpha, v1, beta * c4.y);
+                v2 = fmaf(alpha, v2, beta * c4.z);
+                v3 = fmaf(alpha, v3, beta * c4.w);
             }
         }
     } else {
