@@ -21,8 +21,13 @@
  *     opB = GEMM_OP_T: B stored N x K, op(B)[k][j] = B[j*ldb + k], ldb >= max(1, K)
  *     C stored M x N, C[i][j] at C[i*ldc + j], ldc >= max(1, N)
  *
- * Ownership.  A, B and C are device memory owned by the caller; the library never frees,
- * retains or allocates per call.  C must not overlap A or B.
+ * Ownership.  A, B and C are device memory owned by the caller; the library never frees
+ * or retains them.  C must not overlap A or B.  The library keeps scratch per (device,
+ * stream): a split-K workspace (64 MB and 8192 counters) and two operand buffers for
+ * re-laid-out operands, each allocated when first needed, grown when a larger operand
+ * needs it (after the stream's earlier work), kept until exit, and never allocated while
+ * the stream is being captured (a call then takes a path that needs no new scratch, except
+ * where a 16-bit operand must be packed: see gemm_hgemm_f16f32).
  *
  * Asynchrony.  A call validates its arguments on the host, launches on `stream` (a
  * cudaStream_t passed as void*; NULL means the legacy default stream of the current
@@ -70,6 +75,9 @@ typedef enum {
  * fused multiply-add, never TF32 and never a reduced-precision tensor operation.
  * A, B, C: 4-byte aligned fp32 device pointers; any leading dimension is accepted (the
  * 16-byte vector paths are used only where pointer and leading dimension allow them).
+ * Above 1e10 flops, an operand whose rows run along K (op(A) = N, op(B) = T) may first be
+ * transposed into this stream's scratch buffer (8 bytes of traffic per element) so that
+ * the kernel reads it with 16-byte copies; the result does not depend on it.
  * Limits: M, N, K < 2^31.
  */
 GEMM_API gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
