@@ -36,11 +36,12 @@ constexpr size_t kWsCounters = kWorkspaceCounters;
 // One tile configuration as the host sees it, with its cost-model constants (microseconds,
 // fitted by least squares on log time to 1,600 timed launches on GB300: ten M x N shapes from
 // 256^2 to 3072^2, K = 128 / 513 / 1024 / 4096, op(A) = N and T, every configuration and split
-// count below; the rule picks a plan within 1.6% of the fastest measured one on average).
+// count below; the rule picks a plan within 1.6% of the fastest measured one on average, and
+// within 1.8% over 1,900 launches re-measured after the 128-row tiles moved to 32-wide slices,
+// where a refit gained nothing).
 struct CfgDesc {
-    char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4),
-                // 'X' = 128 x 256 (8 x 16, one CTA per SM)
-    int bm, bn, min_blocks;
+    char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
+    int bm, bn, bk, min_blocks;
     bool a_k_major;  // a K-contiguous A is staged [x][k] (else transposed to [k][x])
     int max_splits;
     double us_slice;   // one K slice of one CTA, per co-resident CTA of the same SM
@@ -56,7 +57,7 @@ template <class C>
 constexpr CfgDesc desc(char name, int max_splits, double us_slice, double us_fixed, double us_split,
                        Launcher l, Launcher ls)
 {
-    return CfgDesc{name, C::BM, C::BN, C::MIN_BLOCKS, mode_allowed<C>(kKVec), max_splits,
+    return CfgDesc{name, C::BM, C::BN, C::BK, C::MIN_BLOCKS, mode_allowed<C>(kKVec), max_splits,
                    us_slice, us_fixed, us_split, l, ls};
 }
 
@@ -64,7 +65,6 @@ const CfgDesc kCfgs[] = {
     desc<CfgL>('L', 4, 1.442, 3.156, 1.764, launch_L, launch_LS),
     desc<CfgM>('M', 12, 0.857, 1.723, 0.464, launch_M, launch_MS),
     desc<CfgS>('S', 16, 0.471, 1.429, 0.015, launch_S, launch_SS),
-    desc<CfgX>('X', 1, 1e9, 0.0, 0.0, launch_X, launch_X),  // outside the model: see choose_plan
 };
 
 const CfgDesc *find_cfg(char name)
@@ -87,21 +87,18 @@ struct Plan {
 // (slices per CTA) * (CTAs on the busiest SM) * us_slice + us_fixed, and every split adds
 // us_split.  Splits come from {1, 2, 3, 4, 6, 8, 12, 16} (at most max_splits, at least two
 // K slices each) and cost 2% extra in the comparison, so near ties keep K whole.
-// The 128 x 256 tile (one CTA per SM) has the best steady state but a large cost per wave
-// that its CTAs cannot hide behind a co-resident CTA; it is taken, unsplit, only for grids of
-// at least 8 waves that fill 94% of their last wave, with K >= 1024 (measured: 16384^2 x 1024
-// 8660 -> 8410 us; at 4096^3, 3.4 waves, it is 11% slower than the 128 x 128 tile).
 // Split-K needs the workspace: at most kWsCounters tiles and kWsBytes of partial tiles.
 // GEMM_GB300_SGEMM_PLAN="S:4" (configuration and splits) overrides the rule, for sweeps; an
 // unsplit override still gets the last-wave split below unless GEMM_GB300_SGEMM_TAIL=0.
 Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool allow_split)
 {
-    // a batch multiplies the tiles (and the split-K partials) of one problem
+    // a batch multiplies the tiles (and the split-K partials) of one problem.  KT counts K in
+    // 16-wide units (the cost model's unit); a configuration splits its own, BK-wide slices.
     const int64_t KT = (K + 15) / 16;
     auto tiles = [&](const CfgDesc &c) { return ((M + c.bm - 1) / c.bm) * ((N + c.bn - 1) / c.bn) * batch; };
     auto fits = [&](const CfgDesc &c, int S) {
-        return S == 1 || (allow_split && S <= KT && S <= c.max_splits && tiles(c) <= int64_t(kWsCounters) &&
-                          size_t(tiles(c)) * S * c.bm * c.bn * 4 <= kWsBytes);
+        return S == 1 || (allow_split && S <= (K + c.bk - 1) / c.bk && S <= c.max_splits &&
+                          tiles(c) <= int64_t(kWsCounters) && size_t(tiles(c)) * S * c.bm * c.bn * 4 <= kWsBytes);
     };
     auto cost = [&](const CfgDesc &c, int S) {
         const int64_t ctas = tiles(c) * S;
@@ -118,7 +115,6 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
     double best = -1.0;
     for (const CfgDesc &c : kCfgs)
         for (int S : kSplits) {
-            if (c.name == 'X') continue;
             if (!fits(c, S) || (S > 1 && KT / S < 2)) continue;
             const double t = cost(c, S);
             if (best < 0.0 || t < best) {
@@ -126,11 +122,6 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
                 plan = {&c, S, 0};
             }
         }
-    const CfgDesc &X = *find_cfg('X');
-    const int64_t tiles_x = tiles(X);
-    const int64_t waves_x = (tiles_x + num_sms - 1) / num_sms;
-    if (K >= 1024 && tiles_x >= 8 * int64_t(num_sms) && double(tiles_x) >= 0.94 * double(waves_x * num_sms))
-        plan = {&X, 1, 0};
     if (const char *e = std::getenv("GEMM_GB300_SGEMM_PLAN")) {
         const CfgDesc *c = find_cfg(e[0]);
         if (c != nullptr && e[1] == ':') {
@@ -153,7 +144,8 @@ Plan choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bo
             double best_rel = 0.4;
             int best_s = 0;
             for (int S = 2; S <= c.max_splits; ++S) {
-                if (KT / S < 4 || size_t(tail) * S * c.bm * c.bn * 4 > kWsBytes) continue;
+                if (KT / S < 4 || S > (K + c.bk - 1) / c.bk || size_t(tail) * S * c.bm * c.bn * 4 > kWsBytes)
+                    continue;
                 const double rel = tail * S <= num_sms ? 1.0 / (2 * S) : (tail * S <= slots ? 1.0 / S : 1.0);
                 if (rel <= best_rel) {
                     best_rel = rel;
@@ -219,7 +211,7 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     // 16-byte aligned base and a leading dimension divisible by 4.
     const bool a_vec = aligned16(A) && lda % 4 == 0 && strides4;
     const bool b_vec = aligned16(B) && ldb % 4 == 0 && strides4;
-    const int KT = static_cast<int>((K + 15) / 16);
+    const int KT = static_cast<int>((K + cfg.bk - 1) / cfg.bk);  // this configuration's slices
     // K-contiguous operands (op(A) = N, op(B) = T): see mode_allowed
     const int a_mode = opA == GEMM_OP_N ? (cfg.a_k_major ? (a_vec ? kKVec : kKScalar) : kKT)
                                         : (a_vec ? kMnVec : kMnScalar);

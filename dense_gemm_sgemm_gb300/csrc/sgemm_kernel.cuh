@@ -5,15 +5,15 @@
 // for Blackwell:
 //   * block tile BM x BN, K sliced by BK and staged in shared memory (copecc "共享内存分块";
 //     ssxxe.cn section "2.1"), as a STAGES-deep cp.async ring instead of the pages'
-//     register double buffer (ssxxe.cn section "2.3") -- the copy engine fills slot s+3
-//     while the FMA units work on slot s, with one __syncthreads per K slice;
+//     register double buffer (ssxxe.cn section "2.3") -- the copies of slice s+STAGES-1 are
+//     in flight while the FMA units work on slice s, with one __syncthreads per K slice;
 //   * each thread owns a TM x TN outer-product tile split into 4 x 4 blocks spaced BM/2
 //     (BN/2) apart (copecc "二维寄存器分块"; ssxxe.cn section "2.2");
-//   * an operand keeps the orientation it has in global memory: rows that run along k
-//     (op(A) = T, op(B) = N) are staged as [k][m] and read with 128-bit loads (copecc
-//     "向量化访存"); rows that run along m or n (op(A) = N, op(B) = T) are staged as [m][k]
-//     and read as k pairs, so every copy is a straight 16-byte (aligned) or 4-byte
-//     (unaligned ld) cp.async and no copy transposes;
+//   * operands whose stored rows run along k (op(A) = T, op(B) = N) are staged [k][x] with
+//     straight copies and read with 128-bit loads (copecc "向量化访存"); K-contiguous ones
+//     (op(A) = N, op(B) = T) are either transposed by 4-byte copies into a [k][x] stage or,
+//     for A on the 4 x 4 tile, staged [x][k] and read four k per 128-bit load; copies are
+//     16 bytes where pointer and leading dimension are aligned, 4 bytes otherwise;
 //   * 16-byte chunk indices are XOR-swizzled (copecc "共享内存填充与重排", Swizzling) so the
 //     copies and the fragment reads hit distinct banks without padding;
 //   * the products are fused multiply-adds on packed fp32 pairs (fma.rn.f32x2 through
@@ -21,8 +21,9 @@
 //   * ragged M, N and K are handled by zero-filled copies (cp.async src-size below the copy
 //     size) and predicated stores (yekq.top "LeetGPU 第二题", the 1001 x 513 x 777 case);
 //   * the 1-D grid is rasterised in groups of tile rows (copecc "线程块网格重排");
-//   * optionally K is split over gridDim.y CTAs whose partial tiles are summed in a fixed
-//     order by the last one to finish (deterministic split-K).
+//   * optionally K is split over several CTAs (for every tile, or for the last partial wave)
+//     whose partial tiles are summed in a fixed order by the last one to finish
+//     (deterministic split-K).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -86,7 +87,7 @@ struct Cfg {
     static_assert(TX % 8 == 0 && TY % 4 == 0, "a warp covers 4 x 8 threads");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "128-bit fragment loads");
     static_assert(BM % 32 == 0 && BN % 32 == 0, "swizzle needs 8 chunks per [k][x] row");
-    static_assert(BK == 16, "[x][k] stages hold four 16-byte chunks per row");
+    static_assert(BK == 16 || TM >= 8, "[x][k] stages (4 x 4 tiles) hold four 16-byte chunks per row");
     static_assert(M_STRIDE % 16 == 0 && N_STRIDE % 16 == 0, "row swizzle repeats every 16 rows");
 };
 
@@ -778,19 +779,20 @@ cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, 
 }
 
 // Tile configurations (one translation unit each, see sgemm_cfg_*.cu).
-using CfgL = Cfg<128, 128, 16, 8, 8, 4, 2>;  // 8 x 8 per thread, two CTAs per SM
-using CfgM = Cfg<128, 64, 16, 8, 4, 4, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
+using CfgL = Cfg<128, 128, 32, 8, 8, 3, 2>;  // 8 x 8 per thread, two CTAs per SM
+using CfgM = Cfg<128, 64, 32, 8, 4, 3, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
 using CfgS = Cfg<64, 64, 16, 4, 4, 4, 3>;    // 4 x 4 per thread, three CTAs per SM
-using CfgX = Cfg<128, 256, 16, 8, 16, 4, 1>; // 8 x 16 per thread, one CTA per SM
-static_assert(CfgL::BK == 16 && CfgM::BK == 16 && CfgS::BK == 16 && CfgX::BK == 16,
-              "the host planner counts K in slices of 16");
+// The 128-row tiles (transposing or [k][x] staging only) take 32-wide K slices in 3 stages:
+// half the per-slice barriers and ring turns of 16-wide slices (128 x 128: 3% faster at
+// 4096^3; 128 x 64: up to 7% at K = 4096).  The 4 x 4 tile keeps 16-wide slices ([x][k]
+// stages of four 16-byte chunks).
+static_assert(CfgS::BK == 16, "the [x][k] fragment loads read 16-wide slices");
 
 // Launchers defined in the configuration translation units.
 cudaError_t launch_L(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_LS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_M(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_MS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
-cudaError_t launch_X(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_S(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_SS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 
