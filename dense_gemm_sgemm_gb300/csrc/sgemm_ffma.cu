@@ -213,7 +213,7 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
     const bool b_vec = aligned16(B) && ldb % 4 == 0 && strides4;
     const int KT = static_cast<int>((K + cfg.bk - 1) / cfg.bk);  // this configuration's slices
     // K-contiguous operands (op(A) = N, op(B) = T): see mode_allowed
-    const int a_mode = opA == GEMM_OP_N ? (cfg.a_k_major ? (a_vec ? kKVec : kKScalar) : kKT)
+    const int a_mode = opA == GEMM_OP_N ? (cfg.a_k_major && a_vec ? kKVec : kKT)
                                         : (a_vec ? kMnVec : kMnScalar);
     const int b_mode = opB == GEMM_OP_T ? kKT : (b_vec ? kMnVec : kMnScalar);
     p.tiles_m = (M + cfg.bm - 1) / cfg.bm;

@@ -126,7 +126,7 @@ extern "C" GEMM_API gemm_status_t gemm_sgemm_f32_noalloc(gemm_op_t opA, gemm_op_
     p.counters = reinterpret_cast<unsigned int *>(scratch);
     p.ws = reinterpret_cast<float *>(scratch + kNoallocCounterBytes);
     const bool a_vec = aligned16(A) && lda % 4 == 0, b_vec = aligned16(B) && ldb % 4 == 0;
-    const int a_mode = opA == GEMM_OP_N ? (a_vec ? kKVec : kKScalar) : (a_vec ? kMnVec : kMnScalar);
+    const int a_mode = opA == GEMM_OP_N ? (a_vec ? kKVec : kKT) : (a_vec ? kMnVec : kMnScalar);
     const int b_mode = opB == GEMM_OP_T ? kKT : (b_vec ? kMnVec : kMnScalar);
     return launch_SS(dev.device, a_mode, b_mode, p, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
