@@ -233,62 +233,50 @@ def time_device(w, dev, steps, warmup, flush, barrier=None):
     return [s.elapsed_time(e) for s, e in ev], wall, launches
 
 
-def time_e2e(w, host, dev, steps):
-    """Through the public API from pinned host buffers: every step copies its inputs in,
-    runs the GEMM and copies its result out.  Steps are pipelined the way a caller streaming
-    independent GEMMs would run them: two device buffer sets, host-to-device copies on one
-    stream, the GEMM on another, device-to-host copies on a third, so the copies of one step
-    overlap the GEMM of its neighbours.  Events order each buffer set's reuse."""
+def time_e2e(w, host, steps, sets=3):
+    """End to end through the public host-memory entry point (gemm_*_host): each step is one
+    call on page-locked host buffers that copies the step's A, B and C_in to the device,
+    runs the GEMM and copies C back, in order on the call's stream.  Steps rotate over
+    three streams, each with its own host buffers (and, inside the library, its own device
+    staging area), the way a caller streaming independent GEMMs would run them: the copies
+    of one step overlap the GEMMs of its neighbours."""
     import torch
 
-    fn = _gemm_fn(w)
+    from dense_gemm_sgemm_gb300 import (gemm_bgemm_bf16f32_host, gemm_hgemm_f16f32_host,
+                                        gemm_sgemm_f32_host)
+
+    fn = {"f32": gemm_sgemm_f32_host, "f16": gemm_hgemm_f16f32_host,
+          "bf16": gemm_bgemm_bf16f32_host}[w.dtype]
+    pinned = [{k: v.pin_memory() for k, v in host.items()} for _ in range(sets)]
+    streams = [torch.cuda.Stream() for _ in range(sets)]
     names = ["A", "B"] + (["C"] if w.beta != 0.0 else [])
-    pinned = [{k: v.pin_memory() for k, v in host.items()} for _ in range(2)]
-    outs = [torch.empty_like(pinned[0]["C"]).pin_memory() for _ in range(2)]
-    bufs = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
     h2d = sum(pinned[0][k].numel() * pinned[0][k].element_size() for k in names)
-    d2h = outs[0].numel() * outs[0].element_size()
-    s_in, s_gemm, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    done_in = [ev(), ev()]
-    done_gemm = [ev(), ev()]
-    done_out = [ev(), ev()]
-    started = [False, False]
+    d2h = w.M * w.N * 4
 
     def step(i):
-        b = i & 1
-        d = bufs[b]
-        with torch.cuda.stream(s_in):
-            if started[b]:  # the set's previous GEMM has read it and its C has been copied out
-                s_in.wait_event(done_gemm[b])
-                s_in.wait_event(done_out[b])
-            for k in names:
-                d[k].copy_(pinned[b][k], non_blocking=True)
-            done_in[b].record(s_in)
-        s_gemm.wait_event(done_in[b])
-        fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, d["A"], w.lda, d["B"], w.ldb, w.beta, d["C"],
-           w.ldc, s_gemm)
-        done_gemm[b].record(s_gemm)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done_gemm[b])
-            outs[b].copy_(d["C"], non_blocking=True)
-            done_out[b].record(s_out)
-        started[b] = True
+        b = pinned[i % sets]
+        fn(w.opA, w.opB, w.M, w.N, w.K, w.alpha, b["A"], w.lda, b["B"], w.ldb, w.beta, b["C"],
+           w.ldc, streams[i % sets])
 
-    for i in range(4):
+    for i in range(2 * sets):  # allocates each stream's staging area
         step(i)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(s_in)
+    t0.record(streams[0])
+    for s in streams[1:]:
+        s.wait_event(t0)
     for i in range(steps):
         step(i)
-    s_in.wait_stream(s_out)
-    t1.record(s_in)
+    for s in streams[1:]:
+        streams[0].wait_stream(s)
+    t1.record(streams[0])
     t1.synchronize()
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(w.flops / (ms * 1e-3) / 1e12, 4), "unit": UNIT,
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "pipelined": "2 buffer sets; copies in, GEMM, copies out on 3 streams"}
+            "d2h_bytes_per_step": int(d2h),
+            "api": f"{fn.__name__} on page-locked host buffers",
+            "pipelined": f"{sets} streams round-robin, each with its own host buffers"}
 
 
 def oracle_sample(w, host, budget_s):
@@ -393,6 +381,9 @@ def run_ours(args, rank, world, local):
         bound, peak = "tensor", peaks["bf16_tflops"]
         peak_src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
     traffic = _traffic_from_profile(kernel, f"{kernel}_{w.name}.txt")
+    # The library's own FFMA-chain probe, run after the timed region: a measured FP32
+    # multiply-add ceiling beside the one derived from unit counts and the maximum clock.
+    probe = round(lib.gemm_measure_fp32_fma_peak(), 2) if w.dtype == "f32" else None
     vs = (round(value / (PAGES_RAGGED_GFLOPS / 1e3), 4)
           if w.name == workloads.sgemm_ragged().name else None)
     line = {
@@ -410,6 +401,7 @@ def run_ours(args, rank, world, local):
                      "peak": round(peak, 2), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": w.algorithmic_bytes, "peak_source": peak_src,
+                     "peak_fma_probe": probe,
                      "median_ms": round(statistics.median(step_ms), 5),
                      "min_ms": round(min(step_ms), 5), "max_ms": round(max(step_ms), 5)},
         "gpu_launches": launches,
@@ -417,7 +409,7 @@ def run_ours(args, rank, world, local):
         "wall_s_timed_region": round(wall, 3),
     }
     e2e_steps = max(3, min(args.steps, 200))
-    line["e2e"] = time_e2e(w, host, dev, e2e_steps)
+    line["e2e"] = time_e2e(w, host, e2e_steps)
     if rank == 0 and not args.no_suite:
         line["suite"] = run_suite(peaks, flush)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

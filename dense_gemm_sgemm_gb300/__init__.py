@@ -10,6 +10,7 @@ in the library's CUDA kernels; torch only owns the memory and the stream.
     gemm_bgemm_bf16f32(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
     gemm_*_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
                            beta, C, ldc, strideC, batch)
+    gemm_*_host(... same as the single calls, A, B, C in host memory ...)
 """
 from __future__ import annotations
 
@@ -20,9 +21,10 @@ from ._lib import GEMM_OP_N, GEMM_OP_T, STATUS, GemmError, library_path, load
 __all__ = [
     "GEMM_OP_N", "GEMM_OP_T", "GemmError", "gemm_sgemm_f32", "gemm_hgemm_f16f32",
     "gemm_bgemm_bf16f32", "gemm_sgemm_f32_strided_batched", "gemm_hgemm_f16f32_strided_batched",
-    "gemm_bgemm_bf16f32_strided_batched", "gemm_sgemm_f32_noalloc",
+    "gemm_bgemm_bf16f32_strided_batched", "gemm_sgemm_f32_noalloc", "gemm_sgemm_f32_host",
+    "gemm_hgemm_f16f32_host", "gemm_bgemm_bf16f32_host",
     "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
-    "gemm_kernel_launches",
+    "gemm_kernel_launches", "gemm_measure_fp32_fma_peak",
     "library_path", "load", "matmul",
 ]
 
@@ -145,6 +147,59 @@ def gemm_sgemm_f32_noalloc(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ld
     _check(st, "gemm_sgemm_f32_noalloc")
 
 
+def _host_addr(x, torch_dtype: str, np_dtypes) -> int:
+    """Address of a host matrix: a CPU torch tensor, a numpy array or an int address."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    import numpy as np
+
+    if isinstance(x, np.ndarray):
+        if x.dtype not in [np.dtype(d) for d in np_dtypes]:
+            raise TypeError(f"expected numpy {np_dtypes}, got {x.dtype}")
+        return x.ctypes.data
+    import torch
+
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("host operands must be CPU torch tensors, numpy arrays or addresses")
+    if x.is_cuda:
+        raise ValueError("the *_host entry points take host memory; use the device calls")
+    if x.dtype != getattr(torch, torch_dtype):
+        raise TypeError(f"expected torch.{torch_dtype}, got {x.dtype}")
+    return x.data_ptr()
+
+
+def _host_call(name, in_dtype, np_in, opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+               stream):
+    st = getattr(load(), name)(_op(opA), _op(opB), M, N, K, alpha,
+                               _host_addr(A, in_dtype, np_in), lda,
+                               _host_addr(B, in_dtype, np_in), ldb, beta,
+                               _host_addr(C, "float32", ["float32"]), ldc, _stream(stream))
+    _check(st, name)
+
+
+def gemm_sgemm_f32_host(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """gemm_sgemm_f32 on host matrices: copies in, GEMM and copy out, in order on the
+    stream; C holds the result once the stream has passed the call (pin the buffers for
+    the call to be asynchronous)."""
+    _host_call("gemm_sgemm_f32_host", "float32", ["float32"], opA, opB, M, N, K, alpha, A, lda,
+               B, ldb, beta, C, ldc, stream)
+
+
+def gemm_hgemm_f16f32_host(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """gemm_hgemm_f16f32 on host matrices (see gemm_sgemm_f32_host)."""
+    _host_call("gemm_hgemm_f16f32_host", "float16", ["float16", "uint16"], opA, opB, M, N, K,
+               alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_bgemm_bf16f32_host(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """gemm_bgemm_bf16f32 on host matrices (see gemm_sgemm_f32_host); numpy operands hold
+    the bfloat16 bit patterns as uint16."""
+    _host_call("gemm_bgemm_bf16f32_host", "bfloat16", ["uint16"], opA, opB, M, N, K, alpha, A,
+               lda, B, ldb, beta, C, ldc, stream)
+
+
 def gemm_get_device_status(stream=None) -> int:
     """Status code of the device error word (waits for the stream, then clears it)."""
     return int(load().gemm_get_device_status(_stream(stream)))
@@ -161,6 +216,15 @@ def gemm_version() -> int:
 def gemm_kernel_launches() -> int:
     """Kernels this process has launched through the library so far (for accounting)."""
     return int(load().gemm_kernel_launches())
+
+
+def gemm_measure_fp32_fma_peak(stream=None) -> float:
+    """Measured FP32 multiply-add throughput of the current device in TFLOP/s (packed FMA
+    chains on every SM, best of three event-timed launches; synchronises the stream)."""
+    out = ctypes.c_double(0.0)
+    _check(load().gemm_measure_fp32_fma_peak(_stream(stream), ctypes.byref(out)),
+           "gemm_measure_fp32_fma_peak")
+    return out.value
 
 
 def gemm_tile_raster(t, tiles_m, tiles_n, log_group):

@@ -37,10 +37,14 @@ SIGNATURES = {
     "gemm_hgemm_f16f32_strided_batched": (_int, _BATCHED_ARGS),
     "gemm_bgemm_bf16f32_strided_batched": (_int, _BATCHED_ARGS),
     "gemm_sgemm_f32_noalloc": (_int, _GEMM_ARGS),
+    "gemm_sgemm_f32_host": (_int, _GEMM_ARGS),
+    "gemm_hgemm_f16f32_host": (_int, _GEMM_ARGS),
+    "gemm_bgemm_bf16f32_host": (_int, _GEMM_ARGS),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_status_string": (ctypes.c_char_p, [_int]),
     "gemm_version": (_int, []),
     "gemm_kernel_launches": (ctypes.c_uint64, []),
+    "gemm_measure_fp32_fma_peak": (_int, [_vp, ctypes.POINTER(ctypes.c_double)]),
     "gemm_tile_raster": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64),
                                 ctypes.POINTER(_i64)]),
 }

@@ -154,9 +154,94 @@ static gemm_status_t tc_impl(int dtype, int opA, int opB, int64_t M, int64_t N, 
                         strideC, batch, st);
 }
 
+// Matrices in host memory: each operand is staged on the device with the caller's leading
+// dimension, so it moves as one contiguous copy (a pitched host-to-device copy of rows this
+// short runs several times slower); then the device path runs on the staged matrices and C
+// comes back, only its M x N elements (a pitched copy when ldc > N leaves the row padding
+// of the caller's C untouched).  Everything is ordered on `stream`.
+template <class T, class DeviceCall>
+static gemm_status_t host_impl(int opA, int opB, int64_t M, int64_t N, int64_t K, float alpha,
+                               const T *A, int64_t lda, const T *B, int64_t ldb, float beta,
+                               float *C, int64_t ldc, void *stream, DeviceCall device_call)
+{
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    gemm_status_t s = check_common(opA, opB, M, N, K, A, lda, B, ldb, C, ldc, need_ab);
+    if (s != GEMM_OK || M == 0 || N == 0) return s;
+    // Elements a rows x cols matrix with leading dimension ld spans; -1 when too large.
+    constexpr int64_t kMaxElems = int64_t(1) << 40;
+    auto extent = [](int64_t rows, int64_t cols, int64_t ld) -> int64_t {
+        if (rows == 0 || cols == 0) return 0;
+        if (ld > 0 && rows - 1 > (kMaxElems - cols) / ld) return -1;
+        return (rows - 1) * ld + cols;
+    };
+    const int64_t nA = need_ab ? extent(opA == GEMM_OP_N ? M : K, opA == GEMM_OP_N ? K : M, lda) : 0;
+    const int64_t nB = need_ab ? extent(opB == GEMM_OP_N ? K : N, opB == GEMM_OP_N ? N : K, ldb) : 0;
+    const int64_t nC = extent(M, N, ldc);
+    if (nA < 0 || nB < 0 || nC < 0) return GEMM_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t bA = up(size_t(nA) * sizeof(T)), bB = up(size_t(nB) * sizeof(T));
+    const size_t bC = up(size_t(nC) * sizeof(float));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(host_staging(dev.device, st, bA + bB + bC));
+    if (base == nullptr) return GEMM_ERR_UNSUPPORTED;
+    T *dA = reinterpret_cast<T *>(base), *dB = reinterpret_cast<T *>(base + bA);
+    float *dC = reinterpret_cast<float *>(base + bA + bB);
+    if ((nA > 0 && cudaMemcpyAsync(dA, A, size_t(nA) * sizeof(T), cudaMemcpyDefault, st) != cudaSuccess) ||
+        (nB > 0 && cudaMemcpyAsync(dB, B, size_t(nB) * sizeof(T), cudaMemcpyDefault, st) != cudaSuccess) ||
+        (beta != 0.0f && cudaMemcpyAsync(dC, C, size_t(nC) * sizeof(float), cudaMemcpyDefault, st) != cudaSuccess)) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    s = device_call(need_ab ? dA : nullptr, need_ab ? dB : nullptr, dC, st);
+    if (s != GEMM_OK) return s;
+    const cudaError_t e =
+        ldc == N ? cudaMemcpyAsync(C, dC, size_t(M) * size_t(N) * sizeof(float), cudaMemcpyDefault, st)
+                 : cudaMemcpy2DAsync(C, size_t(ldc) * sizeof(float), dC, size_t(ldc) * sizeof(float),
+                                     size_t(N) * sizeof(float), size_t(M), cudaMemcpyDefault, st);
+    if (e != cudaSuccess) cudaGetLastError();
+    return from_cuda(e);
+}
+
 }  // namespace gemm
 
 extern "C" {
+
+gemm_status_t gemm_sgemm_f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda, const float *B,
+                                  int64_t ldb, float beta, float *C, int64_t ldc, void *stream)
+{
+    return host_impl(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
+                     [&](const float *dA, const float *dB, float *dC, cudaStream_t st) {
+                         return sgemm_impl(opA, opB, M, N, K, alpha, dA, lda, 0, dB, ldb, 0, beta, dC, ldc,
+                                           0, 1, st);
+                     });
+}
+
+gemm_status_t gemm_hgemm_f16f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                     int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                     const uint16_t *B, int64_t ldb, float beta, float *C,
+                                     int64_t ldc, void *stream)
+{
+    return host_impl(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
+                     [&](const uint16_t *dA, const uint16_t *dB, float *dC, cudaStream_t st) {
+                         return tc_impl(kInF16, opA, opB, M, N, K, alpha, dA, lda, 0, dB, ldb, 0, beta,
+                                        dC, ldc, 0, 1, st);
+                     });
+}
+
+gemm_status_t gemm_bgemm_bf16f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                      int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                      const uint16_t *B, int64_t ldb, float beta, float *C,
+                                      int64_t ldc, void *stream)
+{
+    return host_impl(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
+                     [&](const uint16_t *dA, const uint16_t *dB, float *dC, cudaStream_t st) {
+                         return tc_impl(kInBf16, opA, opB, M, N, K, alpha, dA, lda, 0, dB, ldb, 0, beta,
+                                        dC, ldc, 0, 1, st);
+                     });
+}
 
 gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N, int64_t K,
                              float alpha, const float *A, int64_t lda, const float *B,

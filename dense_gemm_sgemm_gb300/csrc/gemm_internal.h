@@ -48,6 +48,10 @@ bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out);
 // Zeroes the arrival counters of every workspace of device `dev` (after a kernel gave up on
 // a bounded wait and may have left counters raised).  Synchronises those streams.
 void reset_workspace_counters(int dev);
+// Device staging area of at least `bytes` for the host-memory entry points, one per
+// (device, stream), grown by reallocation after synchronising the stream.  nullptr when it
+// would have to be (re)allocated while the stream is being captured, or allocation fails.
+void *host_staging(int dev, cudaStream_t stream, size_t bytes);
 
 // Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
 // A batch of `batch` problems: operand b of problem i starts `stride` elements after that

@@ -1,5 +1,5 @@
-// Per-(device, stream) workspace of the split-K paths of both kernels, and the library's
-// kernel-launch counter.
+// Per-(device, stream) workspace of the split-K paths of both kernels, the per-stream
+// staging area of the host-memory entry points, and the library's kernel-launch counter.
 //
 // One workspace per (device, stream): calls on the same stream are ordered and may share it;
 // calls on different streams never do.  It is allocated once, on the first call on that
@@ -48,6 +48,47 @@ bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out)
     g_ws[{dev, stream}] = w;
     out = w;
     return true;
+}
+
+namespace {
+struct Staging {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_stage_mu;
+std::map<std::pair<int, cudaStream_t>, Staging> g_stage;
+}  // namespace
+
+void *host_staging(int dev, cudaStream_t stream, size_t bytes)
+{
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    Staging &sg = g_stage[{dev, stream}];
+    if (sg.bytes >= bytes && sg.ptr) return sg.ptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (sg.ptr) {
+        // Earlier calls on this stream may still be copying through the old area.
+        if (cudaStreamSynchronize(stream) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cudaFree(sg.ptr);
+        sg.ptr = nullptr;
+        sg.bytes = 0;
+    }
+    // Round up to 2 MiB so a run of slightly larger problems does not reallocate each time.
+    const size_t want = (bytes + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
+    void *p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    sg.ptr = p;
+    sg.bytes = want;
+    return p;
 }
 
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }

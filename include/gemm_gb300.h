@@ -21,13 +21,14 @@
  *     opB = GEMM_OP_T: B stored N x K, op(B)[k][j] = B[j*ldb + k], ldb >= max(1, K)
  *     C stored M x N, C[i][j] at C[i*ldc + j], ldc >= max(1, N)
  *
- * Ownership.  A, B and C are device memory owned by the caller; the library never frees
- * or retains them.  C must not overlap A or B.  The library keeps scratch per (device,
- * stream): a split-K workspace (64 MB and 8192 counters) and two operand buffers for
- * re-laid-out operands, each allocated when first needed, grown when a larger operand
- * needs it (after the stream's earlier work), kept until exit, and never allocated while
- * the stream is being captured (a call then takes a path that needs no new scratch, except
- * where a 16-bit operand must be packed: see gemm_hgemm_f16f32).
+ * Ownership.  A, B and C are device memory owned by the caller (host memory for the
+ * *_host entry points); the library never frees or retains them.  C must not overlap A or
+ * B.  The library keeps scratch per (device, stream): a split-K workspace (64 MB and 8192
+ * counters), two operand buffers for re-laid-out operands and, for the *_host entry points,
+ * a staging area; each is allocated when first needed, grown when a larger problem needs
+ * it (after the stream's earlier work), kept until exit, and never allocated while the
+ * stream is being captured (a call then takes a path that needs no new scratch, except
+ * where a 16-bit operand must be packed -- see gemm_hgemm_f16f32 -- or host matrices staged).
  *
  * Asynchrony.  A call validates its arguments on the host, launches on `stream` (a
  * cudaStream_t passed as void*; NULL means the legacy default stream of the current
@@ -150,6 +151,43 @@ GEMM_API gemm_status_t gemm_bgemm_bf16f32_strided_batched(gemm_op_t opA, gemm_op
                                                           int64_t batch, void *stream);
 
 /*
+ * The three products on matrices in HOST memory: same arguments, layouts, leading-dimension
+ * rules, results and errors as gemm_sgemm_f32, gemm_hgemm_f16f32 and gemm_bgemm_bf16f32,
+ * but A, B and C are host pointers (page-locked, from cudaHostAlloc / cudaHostRegister /
+ * torch pin_memory, for the call to stay asynchronous; pageable memory works too, with the
+ * copies then synchronising as cudaMemcpyAsync does for it).  The source pages have no
+ * counterpart: they copy operands in and results out around the kernel by hand.
+ *
+ * In order on `stream`, the call copies each stored operand -- and C when beta != 0 -- to a
+ * device staging area of this (device, stream) pair as one contiguous copy that keeps the
+ * caller's leading dimension, runs the device GEMM there, and copies the M x N elements of
+ * C back into the caller's C (the row padding of an ldc > N matrix is neither read when
+ * beta == 0 nor ever written).  It returns after enqueueing: A, B and C must stay alive and
+ * unchanged until the stream has passed the call (cudaStreamSynchronize, or an event), and
+ * C holds the result only then.  Calls on different streams overlap on the GPU (the copies
+ * of one with the GEMM of another); calls on one stream run one after the other.
+ *
+ * The staging area is allocated by the first call on a stream and reallocated -- after
+ * synchronising that stream -- when a larger problem arrives; it is kept until the process
+ * exits.  Returns GEMM_ERR_UNSUPPORTED without enqueueing anything when the area would have
+ * to be (re)allocated while the stream is being captured, when device memory for it cannot
+ * be had, or when a matrix spans more than 2^40 elements; GEMM_ERR_LAUNCH when a copy
+ * cannot be enqueued (after the input copies, C may then be partly written or not at all).
+ */
+GEMM_API gemm_status_t gemm_sgemm_f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                           int64_t K, float alpha, const float *A, int64_t lda,
+                                           const float *B, int64_t ldb, float beta, float *C,
+                                           int64_t ldc, void *stream);
+GEMM_API gemm_status_t gemm_hgemm_f16f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                              int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                              const uint16_t *B, int64_t ldb, float beta, float *C,
+                                              int64_t ldc, void *stream);
+GEMM_API gemm_status_t gemm_bgemm_bf16f32_host(gemm_op_t opA, gemm_op_t opB, int64_t M, int64_t N,
+                                               int64_t K, float alpha, const uint16_t *A, int64_t lda,
+                                               const uint16_t *B, int64_t ldb, float beta, float *C,
+                                               int64_t ldc, void *stream);
+
+/*
  * Allocation-free variant of gemm_sgemm_f32, for callers that must not allocate device
  * memory while they run: a framework whose own allocator owns the device memory and
  * forbids other cudaMalloc calls, or a latency-critical caller that cannot afford the
@@ -198,6 +236,18 @@ GEMM_API int gemm_version(void);
  * the difference across a region counts the library's launches in it.  Needs no GPU.
  */
 GEMM_API uint64_t gemm_kernel_launches(void);
+
+/*
+ * Measured FP32 fused multiply-add throughput of the current device, in TFLOP/s (2 flops
+ * per multiply-add), written to *tflops: the strict-FP32 path's roofline denominator, next
+ * to the figure derived from SM count x 128 FP32 lanes x 2 x clock.  A kernel of
+ * independent packed multiply-add chains (fma.rn.f32x2) fills every SM; one untimed launch,
+ * then the best of three launches timed with CUDA events on `stream` (synchronises it;
+ * about a millisecond of GPU time).  Returns GEMM_ERR_INVALID_VALUE for a NULL output,
+ * GEMM_ERR_NO_DEVICE without a current device, GEMM_ERR_LAUNCH when a launch or an event
+ * fails (then *tflops is 0).
+ */
+GEMM_API gemm_status_t gemm_measure_fp32_fma_peak(void *stream, double *tflops);
 
 /*
  * Tile raster used by the kernels (a host function: needs no GPU).  It maps the t-th tile
