@@ -421,8 +421,16 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int ty = (warp / (C::TX / 8)) * 4 + (lane >> 3);
-    const int tx = (warp % (C::TX / 8)) * 8 + (lane & 7);
+    // A warp covers 4 x 8 threads of the thread grid.  A 128-bit shared load costs two
+    // cycles while each group of four consecutive lanes reads at most two distinct 16-byte
+    // chunks, four cycles when it reads four (measured on sm_103a).  The 4 x 4 tiles, whose
+    // inner loop is bound by those loads, therefore lay each lane quad out as a 2 x 2 block
+    // (lane bits 0 and 4 pick the row, bits 1..3 the column): two cycles for both operands
+    // instead of two for A and four for B.  The larger tiles keep rows of eight lanes,
+    // whose address arithmetic needs fewer registers.
+    constexpr bool kQuadBlocks = C::TM * C::TN <= 16;
+    const int ty = (warp / (C::TX / 8)) * 4 + (kQuadBlocks ? ((lane & 1) | ((lane >> 4) << 1)) : (lane >> 3));
+    const int tx = (warp % (C::TX / 8)) * 8 + (kQuadBlocks ? (((lane >> 1) & 1) | (((lane >> 2) & 3) << 1)) : (lane & 7));
 
     int64_t tm, tn;
     raster(tile, p.tiles_m, p.tiles_n, p.log_group, tm, tn);
