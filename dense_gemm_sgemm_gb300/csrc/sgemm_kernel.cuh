@@ -14,8 +14,11 @@
 //     (op(A) = N, op(B) = T) are either transposed by 4-byte copies into a [k][x] stage or,
 //     for A on the 4 x 4 tile, staged [x][k] and read four k per 128-bit load; copies are
 //     16 bytes where pointer and leading dimension are aligned, 4 bytes otherwise;
-//   * 16-byte chunk indices are XOR-swizzled (copecc "共享内存填充与重排", Swizzling) so the
-//     copies and the fragment reads hit distinct banks without padding;
+//   * bank conflicts are avoided as copecc "共享内存填充与重排" describes, both ways: the
+//     128-row tiles XOR-swizzle 16-byte chunk indices (Swizzling, no extra memory); the 4 x 4
+//     tile pads each [k][x] row by one chunk (Padding), which costs 6% more shared memory but
+//     turns every fragment and copy address into a per-thread base plus a constant -- that
+//     tile's inner loop was issue-bound on the swizzle arithmetic;
 //   * the products are fused multiply-adds on packed fp32 pairs (fma.rn.f32x2 through
 //     __ffma2_rn), IEEE fp32 with round-to-nearest-even and no TF32;
 //   * ragged M, N and K are handled by zero-filled copies (cp.async src-size below the copy
@@ -79,7 +82,10 @@ struct Cfg {
     static constexpr int TY = BM / TM, TX = BN / TN;  // thread grid
     static constexpr int MB = TM / 4, NB = TN / 4;    // 4-wide blocks per thread
     static constexpr int M_STRIDE = BM / MB, N_STRIDE = BN / NB;
-    static constexpr int A_STAGE = BK * BM, B_STAGE = BK * BN;  // floats per stage
+    // [k][x] stage rows: the 4 x 4 tiles pad each row by one 16-byte chunk, so every fragment
+    // and copy address is a per-thread base plus a constant; the others XOR-swizzle chunks.
+    static constexpr int PAD = TM * TN <= 16 ? 4 : 0;
+    static constexpr int A_STAGE = BK * (BM + PAD), B_STAGE = BK * (BN + PAD);  // floats per stage
     static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
     static constexpr bool PAIR_M = TM > TN;  // accumulator pairs along the longer side
     static_assert(TY * TX == kThreads, "one thread per TM x TN tile");
@@ -121,9 +127,10 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
 }
 
 // Float offset of element (k, x) in a [BK][W] stage: 16-byte chunk index XOR (k mod 8).
-template <int W>
+template <int W, int PAD>
 __device__ __forceinline__ int swz_mn(int k, int x)
 {
+    if constexpr (PAD > 0) return k * (W + PAD) + x;
     return k * W + ((((x >> 2) ^ (k & 7)) << 2) | (x & 3));
 }
 
@@ -138,12 +145,12 @@ __device__ __forceinline__ int swz_k(int x, int k)
 // only adds the slice offset, so the unrolled copies use immediate offsets.
 //   X    stored matrix, ld its leading dimension (passed to load() from the parameters)
 //   ext  extent of the m (or n) dimension, x0 the tile origin along it
-template <int MODE, int W, int BK>
+template <int MODE, int W, int BK, int PAD>
 struct SliceLoader;
 
 // Stored rows run along k, aligned: 16-byte copies into [k][x].
-template <int W, int BK>
-struct SliceLoader<kMnVec, W, BK> {
+template <int W, int BK, int PAD>
+struct SliceLoader<kMnVec, W, BK, PAD> {
     static constexpr int CPR = W / 4;              // 16-byte chunks per k row
     static constexpr int R = BK * CPR / kThreads;  // copies per thread
     static constexpr int KSTEP = kThreads / CPR;   // k distance between a thread's copies
@@ -160,13 +167,15 @@ struct SliceLoader<kMnVec, W, BK> {
         const int64_t rem = ext - (x0 + 4 * c);
         bytes = rem <= 0 ? 0u : (rem >= 4 ? 16u : static_cast<uint32_t>(rem * 4));
         p = X + kb * ld + (bytes ? x0 + 4 * c : 0);
-        dst0 = static_cast<uint32_t>(kb * W + ((c ^ (kb & 7)) << 2)) * 4u;
+        dst0 = static_cast<uint32_t>(PAD > 0 ? kb * (W + PAD) + 4 * c : kb * W + ((c ^ (kb & 7)) << 2)) * 4u;
     }
     // Byte offset of copy r: rows KSTEP apart keep the swizzle of row kb when KSTEP is a
     // multiple of 8; otherwise each row takes its own.
     __device__ __forceinline__ uint32_t dst(int r) const
     {
-        if constexpr (KSTEP % 8 == 0) {
+        if constexpr (PAD > 0) {
+            return dst0 + r * KSTEP * (W + PAD) * 4;
+        } else if constexpr (KSTEP % 8 == 0) {
             return dst0 + r * KSTEP * W * 4;
         } else {
             const int k = kb + r * KSTEP;
@@ -187,8 +196,8 @@ struct SliceLoader<kMnVec, W, BK> {
 };
 
 // Stored rows run along k, unaligned pointer or ld: 4-byte copies into [k][x].
-template <int W, int BK>
-struct SliceLoader<kMnScalar, W, BK> {
+template <int W, int BK, int PAD>
+struct SliceLoader<kMnScalar, W, BK, PAD> {
     static constexpr int R = BK * W / kThreads;
     static constexpr int KSTEP = kThreads / W;
     static_assert(BK * W % kThreads == 0 && kThreads % W == 0, "");
@@ -211,7 +220,7 @@ struct SliceLoader<kMnScalar, W, BK> {
         for (int r = 0; r < R; ++r) {
             const int k = kb + r * KSTEP;
             const bool ok = x_ok && (FULL || k0 + k < K);
-            cp_async4(stage + static_cast<uint32_t>(swz_mn<W>(k, x)) * 4u, ok ? q + r * KSTEP * ld : base,
+            cp_async4(stage + static_cast<uint32_t>(swz_mn<W, PAD>(k, x)) * 4u, ok ? q + r * KSTEP * ld : base,
                       ok ? 4u : 0u);
         }
     }
@@ -219,8 +228,8 @@ struct SliceLoader<kMnScalar, W, BK> {
 
 // Stored rows run along x (K contiguous), aligned: 16-byte copies into [x][k].  Four
 // consecutive threads take the four chunks of one 64-byte row.
-template <int W, int BK>
-struct SliceLoader<kKVec, W, BK> {
+template <int W, int BK, int PAD>
+struct SliceLoader<kKVec, W, BK, PAD> {
     static constexpr int R = W * 4 / kThreads;  // rows per thread
     static constexpr int XSTEP = kThreads / 4;   // row distance between a thread's copies
     static_assert(W * 4 % kThreads == 0 && XSTEP % 16 == 0, "");
@@ -259,8 +268,8 @@ struct SliceLoader<kKVec, W, BK> {
 // copies a 4 (x) by 8 (k) patch -- lanes 0-3 take four rows of X, lanes in steps of 4 walk
 // 8 consecutive k -- and the swizzle spreads its 32 stores over all 32 banks.  Costs more
 // copy instructions than a K-major stage but keeps the 128-bit fragment reads.
-template <int W, int BK>
-struct SliceLoader<kKT, W, BK> {
+template <int W, int BK, int PAD>
+struct SliceLoader<kKT, W, BK, PAD> {
     static constexpr int RX = W / 32;  // patches per thread along x
     static constexpr int RK = BK / 8;  // patches per thread along k
     static_assert(W % 32 == 0 && BK % 8 == 0 && kThreads == 256, "");
@@ -278,7 +287,8 @@ struct SliceLoader<kKT, W, BK> {
         for (int i = 0; i < RX; ++i)
             if (x0 + xb + 32 * i < ext) row_ok |= 1u << i;
         p = X + (row_ok & 1u ? (x0 + xb) * ld : 0) + kb;
-        dst0 = static_cast<uint32_t>(kb * W + ((warp ^ kb) << 2) + (lane & 3)) * 4u;
+        dst0 = static_cast<uint32_t>(PAD > 0 ? kb * (W + PAD) + 4 * warp + (lane & 3)
+                                             : kb * W + ((warp ^ kb) << 2) + (lane & 3)) * 4u;
     }
     template <bool FULL>
     __device__ __forceinline__ void load(uint32_t stage, const float *base, int64_t ld, int64_t k0,
@@ -291,7 +301,7 @@ struct SliceLoader<kKT, W, BK> {
 #pragma unroll
             for (int rx = 0; rx < RX; ++rx) {
                 const bool ok = k_ok && ((row_ok >> rx) & 1u);
-                cp_async4(stage + dst0 + static_cast<uint32_t>(8 * rk * W + 32 * rx) * 4u,
+                cp_async4(stage + dst0 + static_cast<uint32_t>(8 * rk * (W + PAD) + 32 * rx) * 4u,
                           ok ? q + int64_t(32 * rx) * ld + 8 * rk : base, ok ? 4u : 0u);
             }
         }
@@ -301,13 +311,14 @@ struct SliceLoader<kKT, W, BK> {
 // Fragment loads.  A thread's T values of an operand are 4-wide blocks STRIDE apart,
 // starting at row (or column) 4 * t4 of the tile.
 // [k][x] stages: the values at one k, two 128-bit loads per 8 values.
-template <int W, int T, int STRIDE>
+template <int W, int T, int STRIDE, int PAD>
 __device__ __forceinline__ void load_frag_mn(const float *stage, int k, int t4, float (&v)[T])
 {
 #pragma unroll
     for (int b = 0; b < T / 4; ++b) {
         const int c = (b * STRIDE) / 4 + t4;
-        const float4 f = *reinterpret_cast<const float4 *>(stage + k * W + ((c ^ (k & 7)) << 2));
+        const float4 f = *reinterpret_cast<const float4 *>(
+            stage + (PAD > 0 ? k * (W + PAD) + 4 * c : k * W + ((c ^ (k & 7)) << 2)));
         v[4 * b + 0] = f.x; v[4 * b + 1] = f.y; v[4 * b + 2] = f.z; v[4 * b + 3] = f.w;
     }
 }
@@ -444,8 +455,8 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     const int KT = nsplit > 1 ? min(KT_all - kt0, p.kt_per_split) : KT_all;  // slices of this CTA
 
     const uint32_t sA_addr = smem_addr(sA), sB_addr = smem_addr(sB);
-    const SliceLoader<A_MODE, C::BM, C::BK> la(A, p.lda, p.M, m0, tid);
-    const SliceLoader<B_MODE, C::BN, C::BK> lb(B, p.ldb, p.N, n0, tid);
+    const SliceLoader<A_MODE, C::BM, C::BK, C::PAD> la(A, p.lda, p.M, m0, tid);
+    const SliceLoader<B_MODE, C::BN, C::BK, C::PAD> lb(B, p.ldb, p.N, n0, tid);
     // Copies that read nothing (zero fill) still need a valid address: the parameter-space
     // bases, which cost no registers.
     // On the 4 x 4 tile with 4-byte copies (many copies per FMA), slices that lie wholly
@@ -512,13 +523,13 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
 #pragma unroll
                     for (int i = 0; i < C::TM; ++i) a[i] = ag[kk][i];
                 } else {
-                    load_frag_mn<C::BM, C::TM, C::M_STRIDE>(As, k + kk, ty, a);
+                    load_frag_mn<C::BM, C::TM, C::M_STRIDE, C::PAD>(As, k + kk, ty, a);
                 }
                 if constexpr (is_k_major(B_MODE)) {
 #pragma unroll
                     for (int j = 0; j < C::TN; ++j) b[j] = bg[kk][j];
                 } else {
-                    load_frag_mn<C::BN, C::TN, C::N_STRIDE>(Bs, k + kk, tx, b);
+                    load_frag_mn<C::BN, C::TN, C::N_STRIDE, C::PAD>(Bs, k + kk, tx, b);
                 }
                 acc.fma(a, b);
             }
