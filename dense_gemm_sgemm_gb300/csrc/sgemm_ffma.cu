@@ -38,7 +38,9 @@ constexpr size_t kWsCounters = kWorkspaceCounters;
 // 256^2 to 3072^2, K = 128 / 513 / 1024 / 4096, op(A) = N and T, every configuration and split
 // count below; the rule picks a plan within 1.6% of the fastest measured one on average, and
 // within 1.8% over 1,900 launches re-measured after the 128-row tiles moved to 32-wide slices,
-// where a refit gained nothing).
+// where a refit gained nothing; refit on 3,840 launches -- the same shapes with beta = -0.5
+// and with beta = 0 -- after the 64 x 64 tile's lane-quad layout and padded stages made it
+// faster: 1.4% from the fastest plan on average (geometric), was 2.6%).
 struct CfgDesc {
     char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
     int bm, bn, bk, min_blocks;
@@ -62,9 +64,9 @@ constexpr CfgDesc desc(char name, int max_splits, double us_slice, double us_fix
 }
 
 const CfgDesc kCfgs[] = {
-    desc<CfgL>('L', 4, 1.442, 3.156, 1.764, launch_L, launch_LS),
-    desc<CfgM>('M', 12, 0.857, 1.723, 0.464, launch_M, launch_MS),
-    desc<CfgS>('S', 16, 0.471, 1.429, 0.015, launch_S, launch_SS),
+    desc<CfgL>('L', 4, 1.348, 2.682, 1.846, launch_L, launch_LS),
+    desc<CfgM>('M', 12, 0.791, 2.395, 0.725, launch_M, launch_MS),
+    desc<CfgS>('S', 16, 0.403, 1.511, 0.150, launch_S, launch_SS),
 };
 
 const CfgDesc *find_cfg(char name)
