@@ -40,7 +40,9 @@ constexpr size_t kWsCounters = kWorkspaceCounters;
 // within 1.8% over 1,900 launches re-measured after the 128-row tiles moved to 32-wide slices,
 // where a refit gained nothing; refit on 3,840 launches -- the same shapes with beta = -0.5
 // and with beta = 0 -- after the 64 x 64 tile's lane-quad layout and padded stages made it
-// faster: 1.4% from the fastest plan on average (geometric), was 2.6%).
+// faster: 1.4% from the fastest plan on average (geometric), was 2.6%; 1.6% on 3,840
+// launches re-measured after the 128 x 64 tile moved to padded 16-wide slices, where a refit
+// gained nothing).
 struct CfgDesc {
     char name;  // 'L' = 128 x 128 (8 x 8 per thread), 'M' = 128 x 64 (8 x 4), 'S' = 64 x 64 (4 x 4)
     int bm, bn, bk, min_blocks;

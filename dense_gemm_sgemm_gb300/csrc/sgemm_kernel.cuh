@@ -82,9 +82,10 @@ struct Cfg {
     static constexpr int TY = BM / TM, TX = BN / TN;  // thread grid
     static constexpr int MB = TM / 4, NB = TN / 4;    // 4-wide blocks per thread
     static constexpr int M_STRIDE = BM / MB, N_STRIDE = BN / NB;
-    // [k][x] stage rows: the 4 x 4 tiles pad each row by one 16-byte chunk, so every fragment
-    // and copy address is a per-thread base plus a constant; the others XOR-swizzle chunks.
-    static constexpr int PAD = TM * TN <= 16 ? 4 : 0;
+    // [k][x] stage rows: the 4 x 4 and 8 x 4 tiles pad each row by one 16-byte chunk, so every
+    // fragment and copy address is a per-thread base plus a constant; the 8 x 8 tile, whose
+    // register budget has room for the swizzle arithmetic, XOR-swizzles chunks.
+    static constexpr int PAD = TM * TN <= 32 ? 4 : 0;
     static constexpr int A_STAGE = BK * (BM + PAD), B_STAGE = BK * (BN + PAD);  // floats per stage
     static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
     static constexpr bool PAIR_M = TM > TN;  // accumulator pairs along the longer side
@@ -438,12 +439,12 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     const int lane = tid & 31, warp = tid >> 5;
     // A warp covers 4 x 8 threads of the thread grid.  A 128-bit shared load costs two
     // cycles while each group of four consecutive lanes reads at most two distinct 16-byte
-    // chunks, four cycles when it reads four (measured on sm_103a).  The 4 x 4 tiles, whose
-    // inner loop is bound by those loads, therefore lay each lane quad out as a 2 x 2 block
-    // (lane bits 0 and 4 pick the row, bits 1..3 the column): two cycles for both operands
-    // instead of two for A and four for B.  The larger tiles keep rows of eight lanes,
-    // whose address arithmetic needs fewer registers.
-    constexpr bool kQuadBlocks = C::TM * C::TN <= 16;
+    // chunks, four cycles when it reads four (measured on sm_103a).  The 4 x 4 and 8 x 4
+    // tiles, whose inner loops are bound by those loads, therefore lay each lane quad out as
+    // a 2 x 2 block (lane bits 0 and 4 pick the row, bits 1..3 the column): two cycles for
+    // both operands instead of two for A and four for B.  The 8 x 8 tile keeps rows of eight
+    // lanes: there the quad layout made ptxas spill.
+    constexpr bool kQuadBlocks = C::TM * C::TN <= 32;
     const int ty = (warp / (C::TX / 8)) * 4 + (kQuadBlocks ? ((lane & 1) | ((lane >> 4) << 1)) : (lane >> 3));
     const int tx = (warp % (C::TX / 8)) * 8 + (kQuadBlocks ? (((lane >> 1) & 1) | (((lane >> 2) & 3) << 1)) : (lane & 7));
 
@@ -777,12 +778,14 @@ cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, 
 
 // Tile configurations (one translation unit each, see sgemm_cfg_*.cu).
 using CfgL = Cfg<128, 128, 32, 8, 8, 3, 2>;  // 8 x 8 per thread, two CTAs per SM
-using CfgM = Cfg<128, 64, 32, 8, 4, 3, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
+using CfgM = Cfg<128, 64, 16, 8, 4, 4, 3>;   // 8 x 4 per thread (pairs along m), three CTAs per SM
 using CfgS = Cfg<64, 64, 16, 4, 4, 4, 3>;    // 4 x 4 per thread, three CTAs per SM
-// The 128-row tiles (transposing or [k][x] staging only) take 32-wide K slices in 3 stages:
-// half the per-slice barriers and ring turns of 16-wide slices (128 x 128: 3% faster at
-// 4096^3; 128 x 64: up to 7% at K = 4096).  The 4 x 4 tile keeps 16-wide slices ([x][k]
-// stages of four 16-byte chunks).
+// The 128 x 128 tile takes 32-wide K slices in 3 stages: half the per-slice barriers and ring
+// turns of 16-wide slices (3% faster at 4096^3).  The 128 x 64 tile had them too (up to 7% at
+// K = 4096 against swizzled 16-wide slices), but three CTAs per SM of padded 32-wide stages do
+// not fit in shared memory, and padded 16-wide slices in 4 stages beat both (768 x 1024 x 513:
+// 41.6 -> 35.6 us, 1536^2 x 513: 66.2 -> 62.1 us).  The 4 x 4 tile keeps 16-wide slices
+// ([x][k] stages of four 16-byte chunks).
 static_assert(CfgS::BK == 16, "the [x][k] fragment loads read 16-wide slices");
 
 // Launchers defined in the configuration translation units.
