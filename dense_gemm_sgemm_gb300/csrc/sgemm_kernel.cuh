@@ -15,10 +15,10 @@
 //     for A on the 4 x 4 tile, staged [x][k] and read four k per 128-bit load; copies are
 //     16 bytes where pointer and leading dimension are aligned, 4 bytes otherwise;
 //   * bank conflicts are avoided as copecc "共享内存填充与重排" describes, both ways: the
-//     128-row tiles XOR-swizzle 16-byte chunk indices (Swizzling, no extra memory); the 4 x 4
-//     tile pads each [k][x] row by one chunk (Padding), which costs 6% more shared memory but
-//     turns every fragment and copy address into a per-thread base plus a constant -- that
-//     tile's inner loop was issue-bound on the swizzle arithmetic;
+//     128 x 128 tile XOR-swizzles 16-byte chunk indices (Swizzling, no extra memory); the
+//     4 x 4 and 8 x 4 tiles pad each [k][x] row by one chunk (Padding), which costs 6% more
+//     shared memory but turns every fragment and copy address into a per-thread base plus a
+//     constant -- their inner loops were issue-bound on the swizzle arithmetic;
 //   * the products are fused multiply-adds on packed fp32 pairs (fma.rn.f32x2 through
 //     __ffma2_rn), IEEE fp32 with round-to-nearest-even and no TF32;
 //   * ragged M, N and K are handled by zero-filled copies (cp.async src-size below the copy
