@@ -237,6 +237,13 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
             if (e != cudaSuccess) return e;
             p.cta_offset = plan.full_tiles;
         }
+        // Two splits of every 64 x 64 tile: the pair forms a cluster and hands its partial
+        // over through distributed shared memory instead of the workspace (the same sum,
+        // p0 + p1).  GEMM_GB300_SGEMM_PAIR=0 keeps the workspace hand-off (for tests).
+        if (plan.splits == 2 && plan.full_tiles == 0 && cfg.name == 'S') {
+            const char *e = std::getenv("GEMM_GB300_SGEMM_PAIR");
+            if (e == nullptr || e[0] != '0') return launch_SP(dev.device, a_mode, b_mode, p, stream);
+        }
         return cfg.launch_split(dev.device, a_mode, b_mode, p, stream);
     }
     return cfg.launch(dev.device, a_mode, b_mode, p, stream);

@@ -127,6 +127,30 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Thread-block cluster helpers (the two K splits of a tile in one cluster).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // Float offset of element (k, x) in a [BK][W] stage: 16-byte chunk index XOR (k mod 8).
 template <int W, int PAD>
 __device__ __forceinline__ int swz_mn(int k, int x)
@@ -399,12 +423,14 @@ struct Acc {
     }
 };
 
-template <class C, int A_MODE, int B_MODE, bool SPLIT>
+template <class C, int A_MODE, int B_MODE, bool SPLIT, bool PAIR>
 __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
                                            const float *__restrict__ B, float *__restrict__ Cmat,
                                            int64_t tile, int split, int nsplit, int64_t slot);
 
-template <class C, int A_MODE, int B_MODE, bool SPLIT>
+// PAIR: every tile is split in two and the launch forms clusters of two CTAs, the two splits
+// of one tile (cluster rank = split); see the hand-off in sgemm_tile.
+template <class C, int A_MODE, int B_MODE, bool SPLIT, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(const SgemmParams p)
 {
     // One problem per CTA: problem blockIdx.z of this launch (the host launches batches of
@@ -420,17 +446,18 @@ __global__ void __launch_bounds__(kThreads, C::MIN_BLOCKS) sgemm_ffma_kernel(con
         nsplit = p.splits;
         slot = z * (p.tiles_m * p.tiles_n - p.full_tiles) + (tile - p.full_tiles);
     }
-    sgemm_tile<C, A_MODE, B_MODE, SPLIT>(p, p.A + z * p.stride_a, p.B + z * p.stride_b, p.C + z * p.stride_c,
-                                         tile, split, nsplit, slot);
+    sgemm_tile<C, A_MODE, B_MODE, SPLIT, PAIR>(p, p.A + z * p.stride_a, p.B + z * p.stride_b,
+                                               p.C + z * p.stride_c, tile, split, nsplit, slot);
 }
 
 // One output tile (or one K split of it) of one problem.  slot numbers the split tile's
 // partials and arrival counter among all split tiles of the launch.
-template <class C, int A_MODE, int B_MODE, bool SPLIT>
+template <class C, int A_MODE, int B_MODE, bool SPLIT, bool PAIR>
 __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__restrict__ A,
                                            const float *__restrict__ B, float *__restrict__ Cmat,
                                            int64_t tile, int split, int nsplit, int64_t slot)
 {
+    static_assert(!PAIR || (SPLIT && C::TM * C::TN <= 16), "cluster pairs: split 4 x 4 tiles");
     extern __shared__ __align__(16) float smem[];
     float *sA = smem;
     float *sB = smem + C::STAGES * C::A_STAGE;
@@ -570,10 +597,41 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
         }
     };
     if constexpr (kSmallTile) {
-        if (beta != 0.0f) read_c();
+        if (beta != 0.0f && (!PAIR || split == 0)) read_c();
     }
 
-    if (SPLIT && nsplit > 1) {
+    if constexpr (PAIR) {
+        // The two K splits of this tile are one cluster.  Split 1 leaves its partial tile in
+        // its own (now idle) operand ring, thread-major; after a cluster barrier split 0 reads
+        // it through distributed shared memory, adds it to its own (p0 + p1, the order of the
+        // global hand-off below) and writes C; a second barrier keeps split 1's shared memory
+        // alive until then.  No global round trip, fence or arrival counter.  Both CTAs of a
+        // cluster are resident together, and both pass both barriers on every path.
+        constexpr int Q = C::TM * C::TN / 4;  // float4 per thread
+        constexpr int QR = C::TN / 4;         // float4 per accumulator row
+        __syncthreads();  // every warp is done reading the ring
+        float4 *part = reinterpret_cast<float4 *>(smem);
+        if (split == 1) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int i = q / QR, j = 4 * (q % QR);
+                part[q * kThreads + tid] = make_float4(acc.at(i, j), acc.at(i, j + 1), acc.at(i, j + 2), acc.at(i, j + 3));
+            }
+        }
+        cluster_sync();
+        if (split == 1) {
+            cluster_sync();
+            return;
+        }
+        const uint32_t peer = map_to_rank(smem_addr(part), 1u);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const float4 u = ld_cluster_f4(peer + static_cast<uint32_t>(q * kThreads + tid) * 16u);
+            const int i = q / QR, j = 4 * (q % QR);
+            acc.at(i, j) += u.x; acc.at(i, j + 1) += u.y; acc.at(i, j + 2) += u.z; acc.at(i, j + 3) += u.w;
+        }
+        cluster_sync();
+    } else if (SPLIT && nsplit > 1) {
         // Deterministic split-K: every split stores its partial tile, and the split that
         // arrives last adds all partials in split order 0, 1, ..., splits-1 -- the same
         // order whichever CTA finishes last -- before the epilogue.
@@ -691,10 +749,10 @@ __device__ __forceinline__ void sgemm_tile(const SgemmParams &p, const float *__
     }
 }
 
-template <class C, bool SPLIT, int A_MODE, int B_MODE>
+template <class C, bool SPLIT, int A_MODE, int B_MODE, bool PAIR = false>
 cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
 {
-    auto kern = sgemm_ffma_kernel<C, A_MODE, B_MODE, SPLIT>;
+    auto kern = sgemm_ffma_kernel<C, A_MODE, B_MODE, SPLIT, PAIR>;
     // The shared-memory opt-in is a per-device function attribute: set it once per device.
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = uint64_t(1) << (dev_id & 63);
@@ -718,9 +776,29 @@ cudaError_t launch_cfg(int dev_id, const SgemmParams &p, cudaStream_t stream)
         q.B = p.B + b0 * p.stride_b;
         q.C = p.C + b0 * p.stride_c;
         const dim3 grid(static_cast<unsigned>(ctas), 1u, static_cast<unsigned>(q.batch));
-        kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(q);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if constexpr (PAIR) {
+            // Clusters of the two splits of a tile (CTAs 2t and 2t + 1 of the grid).
+            if (p.splits != 2 || p.full_tiles != 0 || p.cta_offset != 0 || ctas % 2 != 0)
+                return cudaErrorInvalidValue;
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr{};
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
+            if (e != cudaSuccess) return e;
+        } else {
+            kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(q);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         count_launches();
     }
     return cudaSuccess;
@@ -740,38 +818,39 @@ constexpr bool mode_allowed(int mode)
     return mode == kMnVec || mode == kMnScalar || mode == kKVec || mode == kKT;
 }
 
-template <class C, bool SPLIT, int A_MODE, int B_MODE>
+template <class C, bool SPLIT, int A_MODE, int B_MODE, bool PAIR>
 cudaError_t launch_if_allowed(int dev_id, const SgemmParams &p, cudaStream_t s)
 {
     if constexpr (mode_allowed<C>(A_MODE) && mode_allowed<C>(B_MODE))
-        return launch_cfg<C, SPLIT, A_MODE, B_MODE>(dev_id, p, s);
+        return launch_cfg<C, SPLIT, A_MODE, B_MODE, PAIR>(dev_id, p, s);
     else
         return cudaErrorInvalidValue;
 }
 
-template <class C, bool SPLIT, int A_MODE>
+template <class C, bool SPLIT, int A_MODE, bool PAIR>
 cudaError_t launch_b(int dev_id, int b_mode, const SgemmParams &p, cudaStream_t s)
 {
     switch (b_mode) {
-    case kMnVec: return launch_if_allowed<C, SPLIT, A_MODE, kMnVec>(dev_id, p, s);
-    case kMnScalar: return launch_if_allowed<C, SPLIT, A_MODE, kMnScalar>(dev_id, p, s);
-    case kKVec: return launch_if_allowed<C, SPLIT, A_MODE, kKVec>(dev_id, p, s);
-    case kKT: return launch_if_allowed<C, SPLIT, A_MODE, kKT>(dev_id, p, s);
+    case kMnVec: return launch_if_allowed<C, SPLIT, A_MODE, kMnVec, PAIR>(dev_id, p, s);
+    case kMnScalar: return launch_if_allowed<C, SPLIT, A_MODE, kMnScalar, PAIR>(dev_id, p, s);
+    case kKVec: return launch_if_allowed<C, SPLIT, A_MODE, kKVec, PAIR>(dev_id, p, s);
+    case kKT: return launch_if_allowed<C, SPLIT, A_MODE, kKT, PAIR>(dev_id, p, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 // Launches configuration C for the given staging modes.  p.tiles_m/tiles_n, p.splits and
-// p.kt_per_split must already describe the grid of C.
-template <class C, bool SPLIT>
+// p.kt_per_split must already describe the grid of C.  PAIR: two splits per tile as
+// two-CTA clusters (p.splits == 2, every tile split).
+template <class C, bool SPLIT, bool PAIR = false>
 cudaError_t launch_ab(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s)
 {
     if (!mode_allowed<C>(a_mode)) return cudaErrorInvalidValue;
     switch (a_mode) {
-    case kMnVec: return launch_b<C, SPLIT, kMnVec>(dev_id, b_mode, p, s);
-    case kMnScalar: return launch_b<C, SPLIT, kMnScalar>(dev_id, b_mode, p, s);
-    case kKVec: return launch_b<C, SPLIT, kKVec>(dev_id, b_mode, p, s);
-    case kKT: return launch_b<C, SPLIT, kKT>(dev_id, b_mode, p, s);
+    case kMnVec: return launch_b<C, SPLIT, kMnVec, PAIR>(dev_id, b_mode, p, s);
+    case kMnScalar: return launch_b<C, SPLIT, kMnScalar, PAIR>(dev_id, b_mode, p, s);
+    case kKVec: return launch_b<C, SPLIT, kKVec, PAIR>(dev_id, b_mode, p, s);
+    case kKT: return launch_b<C, SPLIT, kKT, PAIR>(dev_id, b_mode, p, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -795,6 +874,7 @@ cudaError_t launch_M(int dev_id, int a_mode, int b_mode, const SgemmParams &p, c
 cudaError_t launch_MS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_S(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 cudaError_t launch_SS(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
+cudaError_t launch_SP(int dev_id, int a_mode, int b_mode, const SgemmParams &p, cudaStream_t s);
 
 }  // namespace sg
 }  // namespace gemm

@@ -86,7 +86,7 @@ def test_fuzz_shapes_ops_padding(opA, opB):
 
 # Every tile configuration (L 128 x 128, M 128 x 64, S 64 x 64), with and without split K,
 # through the plan override, on shapes with ragged tails in M, N and K and both copy widths.
-@pytest.mark.parametrize("plan", ["L:1", "L:3", "M:1", "M:2", "M:5", "S:1", "S:3", "S:6"])
+@pytest.mark.parametrize("plan", ["L:1", "L:3", "M:1", "M:2", "M:5", "S:1", "S:2", "S:3", "S:6"])
 def test_every_tile_configuration(plan, monkeypatch):
     monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", plan)
     for i, (opA, opB) in enumerate(itertools.product("NT", "NT")):
@@ -101,6 +101,47 @@ def test_every_tile_configuration(plan, monkeypatch):
                                 seed=300 + i, dist_a="int4", dist_b="int4")
         inputs, dev = _run(wi)
         parity.check_full(wi, inputs, dev["C"], integer=True)
+
+
+# Two K splits of every 64 x 64 tile run as two-CTA clusters that hand the partial over
+# through distributed shared memory; the workspace hand-off sums in the same order (p0 + p1),
+# so both give the same bits -- on the ragged headline shape (both operands with 4-byte
+# copies), an aligned batch and a shape whose second split has fewer slices.
+@pytest.mark.parametrize("shape", [(1001, 777, 513, "N", "N", 1), (512, 384, 1024, "T", "N", 3),
+                                   (130, 200, 48, "N", "T", 1)])
+def test_cluster_pair_split_matches_workspace_split(shape, monkeypatch):
+    M, N, K, opA, opB, batch = shape
+    monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", "S:2")
+    w = workloads.Workload(f"pair_{M}x{N}x{K}", "f32", M, N, K, opA, opB, alpha=1.5, beta=-0.5,
+                           seed=91)
+    inputs = workloads.make_inputs(w)
+    outs = []
+    for pair in ("1", "0"):
+        monkeypatch.setenv("GEMM_GB300_SGEMM_PAIR", pair)
+        _, dev = _run(w, inputs)
+        outs.append(dev["C"].cpu())
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    parity.check_full(w, inputs, outs[0].cuda())
+    if batch > 1:
+        # strided batch of `batch` problems through the same plan: each equals its single call
+        from dense_gemm_sgemm_gb300 import gemm_sgemm_f32_strided_batched
+
+        g = torch.Generator().manual_seed(92)
+        a_shape, b_shape = w.a_shape, w.b_shape
+        A = torch.rand(batch, *a_shape, generator=g) * 2 - 1
+        B = torch.rand(batch, *b_shape, generator=g) * 2 - 1
+        Cin = torch.rand(batch, M, N, generator=g) * 2 - 1
+        res = []
+        for pair in ("1", "0"):
+            monkeypatch.setenv("GEMM_GB300_SGEMM_PAIR", pair)
+            dC = Cin.cuda()
+            gemm_sgemm_f32_strided_batched(opA, opB, M, N, K, 1.5, A.cuda(), a_shape[1],
+                                           a_shape[0] * a_shape[1], B.cuda(), b_shape[1],
+                                           b_shape[0] * b_shape[1], -0.5, dC, N, M * N, batch)
+            torch.cuda.synchronize()
+            assert gemm_get_device_status() == 0
+            res.append(dC.cpu())
+        assert torch.equal(res[0].view(torch.int32), res[1].view(torch.int32))
 
 
 # An unsplit 128 x 128 plan whose last wave is small runs that wave's tiles as K splits in a
