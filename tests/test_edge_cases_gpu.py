@@ -126,3 +126,26 @@ def test_bf16_wide_exponent_range():
     got = _gemm("bf16", "N", "N", M, N, K, 1.0, A, B, 0.0, C).numpy()
     ref, absdot = _oracle("bf16", "N", "N", M, N, K, 1.0, A, B, 0.0, C)
     parity.assert_close(w, got, ref, absdot, None)
+
+
+@pytest.mark.parametrize("dtype,plan", [("f32", "L:1"), ("f32", "L:3"), ("f32", "M:2"), ("f32", "S:1"),
+                                        ("f32", "S:2"), ("f32", "S:5"), ("f16", None), ("bf16", None)])
+def test_writes_stay_inside_c(dtype, plan, monkeypatch):
+    # C is the first M rows of a larger NaN-filled buffer with padded rows (ldc > N): after
+    # the call every element outside the M x N matrix -- the row padding and two guard rows
+    # after it -- must still be NaN, on every tile configuration and split path.
+    if plan:
+        monkeypatch.setenv("GEMM_GB300_SGEMM_PLAN", plan)
+    M, N, K, ldc = 333, 290, 200, 301
+    g = torch.Generator().manual_seed(67)
+    A = (torch.rand(M, K, generator=g) * 2 - 1).to(TORCH[dtype])
+    B = (torch.rand(K, N, generator=g) * 2 - 1).to(TORCH[dtype])
+    buf = torch.full(((M + 2) * ldc,), float("nan"), device="cuda")
+    C = buf[: M * ldc].view(M, ldc)
+    FN[dtype]("N", "N", M, N, K, 1.0, A.cuda(), K, B.cuda(), N, 0.0, C, ldc)
+    torch.cuda.synchronize()
+    assert gemm_get_device_status() == 0
+    full = buf.view(M + 2, ldc).cpu()
+    assert not torch.isnan(full[:M, :N]).any()
+    assert torch.isnan(full[:M, N:]).all(), "row padding written"
+    assert torch.isnan(full[M:]).all(), "guard rows after C written"

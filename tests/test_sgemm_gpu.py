@@ -97,6 +97,8 @@ def test_every_tile_configuration(plan, monkeypatch):
                                    seed=200 + 4 * i + j, pad=pad)
             inputs, dev = _run(w)
             parity.check_full(w, inputs, dev["C"][:, : w.N].contiguous() if pad[2] else dev["C"])
+            if pad[2]:
+                assert torch.isnan(dev["C"][:, w.N:]).all(), "row padding of C was written"
         wi = workloads.Workload(f"plan{plan}_int_{opA}{opB}", "f32", 257, 191, 515, opA, opB,
                                 seed=300 + i, dist_a="int4", dist_b="int4")
         inputs, dev = _run(wi)
