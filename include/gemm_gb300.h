@@ -40,8 +40,10 @@
  * K == 0 or alpha == 0: C = beta * C.  beta == 0: C is written without being read, so
  * NaN or Inf already in C does not propagate.  alpha and beta are host values.
  *
- * Thread safety.  Calls may come from several host threads; calls that write the same C
- * concurrently race, as with any BLAS.
+ * Thread safety.  Calls may come from several host threads.  Calls on one stream from
+ * different threads must not overlap in time (a call may grow that stream's scratch while
+ * the other enqueues work that uses it); calls that write the same C concurrently race, as
+ * with any BLAS.
  */
 #ifndef GEMM_GB300_H
 #define GEMM_GB300_H
@@ -169,7 +171,7 @@ GEMM_API gemm_status_t gemm_bgemm_bf16f32_strided_batched(gemm_op_t opA, gemm_op
  *
  * The staging area is allocated by the first call on a stream and reallocated -- after
  * synchronising that stream -- when a larger problem arrives; it is kept until the process
- * exits.  Returns GEMM_ERR_UNSUPPORTED without enqueueing anything when the area would have
+ * exits (see Thread safety above for calls sharing a stream).  Returns GEMM_ERR_UNSUPPORTED without enqueueing anything when the area would have
  * to be (re)allocated while the stream is being captured, when device memory for it cannot
  * be had, or when a matrix spans more than 2^40 elements; GEMM_ERR_LAUNCH when a copy
  * cannot be enqueued (after the input copies, C may then be partly written or not at all).
