@@ -98,3 +98,34 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 4)
     with pytest.raises(ValueError):
         g.gemm_sgemm_f32("N", "N", 4, 4, 4, 1.0, x, 4, x, 4, 0.0, x, 4, stream=0)
+
+
+def test_host_entry_validation_needs_no_device(lib):
+    # The *_host entry points validate like the device calls before any copy or allocation.
+    P = 4096  # never dereferenced: every call below returns first
+    for f in (lib.gemm_sgemm_f32_host, lib.gemm_hgemm_f16f32_host, lib.gemm_bgemm_bf16f32_host):
+        assert f(2, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 1      # bad op
+        assert f(0, 0, 4, 4, 4, 1.0, P, 3, P, 4, 0.0, P, 4, None) == 1      # lda < K
+        assert f(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 3, None) == 1      # ldc < N
+        assert f(0, 0, 4, 4, 4, 1.0, None, 4, P, 4, 0.0, P, 4, None) == 1   # NULL A
+        assert f(0, 0, 4, 4, 4, 1.0, P, 4, P, 4, 0.0, None, 4, None) == 1   # NULL C
+        assert f(0, 0, 0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, None) == 0  # empty: nothing
+        assert f(0, 0, 1 << 31, 4, 4, 1.0, P, 4, P, 4, 0.0, P, 4, None) == 3
+
+
+def test_binding_host_entry_refuses_wrong_types(lib):
+    import numpy as np
+    import torch
+
+    a = np.zeros((4, 4), dtype=np.float64)
+    with pytest.raises(TypeError):
+        g.gemm_sgemm_f32_host("N", "N", 4, 4, 4, 1.0, a, 4, a, 4, 0.0, a, 4, stream=0)
+    with pytest.raises(TypeError):
+        t = torch.zeros(4, 4, dtype=torch.float16)
+        g.gemm_sgemm_f32_host("N", "N", 4, 4, 4, 1.0, t, 4, t, 4, 0.0, t, 4, stream=0)
+    with pytest.raises(TypeError):
+        g.gemm_sgemm_f32_host("N", "N", 4, 4, 4, 1.0, [1.0], 4, [1.0], 4, 0.0, [1.0], 4, stream=0)
+
+
+def test_fma_peak_probe_rejects_a_null_output_without_a_device(lib):
+    assert lib.gemm_measure_fp32_fma_peak(None, ctypes.POINTER(ctypes.c_double)()) == 1
