@@ -26,7 +26,10 @@
 //   * the 1-D grid is rasterised in groups of tile rows (copecc "线程块网格重排");
 //   * optionally K is split over several CTAs (for every tile, or for the last partial wave)
 //     whose partial tiles are summed in a fixed order by the last one to finish
-//     (deterministic split-K).
+//     (deterministic split-K); two splits of a 4 x 4-thread tile instead form a two-CTA
+//     cluster and the first reads the second's partial from its shared memory (same order);
+//   * each lane quad of the 4 x 4 and 8 x 4 tiles is a 2 x 2 block of the thread grid, so a
+//     128-bit fragment load reads at most two distinct 16-byte chunks per quad (2 cycles).
 #pragma once
 
 #include <cuda_runtime.h>
