@@ -24,7 +24,7 @@ __all__ = [
     "gemm_bgemm_bf16f32_strided_batched", "gemm_sgemm_f32_noalloc", "gemm_sgemm_f32_host",
     "gemm_hgemm_f16f32_host", "gemm_bgemm_bf16f32_host",
     "gemm_get_device_status", "gemm_status_string", "gemm_version", "gemm_tile_raster",
-    "gemm_kernel_launches", "gemm_measure_fp32_fma_peak",
+    "gemm_kernel_launches", "gemm_measure_fp32_fma_peak", "gemm_sgemm_configs",
     "library_path", "load", "matmul",
 ]
 
@@ -225,6 +225,21 @@ def gemm_measure_fp32_fma_peak(stream=None) -> float:
     _check(load().gemm_measure_fp32_fma_peak(_stream(stream), ctypes.byref(out)),
            "gemm_measure_fp32_fma_peak")
     return out.value
+
+
+def gemm_sgemm_configs():
+    """The strict-FP32 path's tile configurations as dicts (host function, no GPU)."""
+    from ._lib import SgemmConfig
+
+    out, i = [], 0
+    while True:
+        c = SgemmConfig()
+        if load().gemm_sgemm_config(i, ctypes.byref(c)) != 0:
+            return out
+        d = {f: getattr(c, f) for f, _ in SgemmConfig._fields_}
+        d["name"] = d["name"].decode()
+        out.append(d)
+        i += 1
 
 
 def gemm_tile_raster(t, tiles_m, tiles_n, log_group):

@@ -47,7 +47,14 @@ SIGNATURES = {
     "gemm_measure_fp32_fma_peak": (_int, [_vp, ctypes.POINTER(ctypes.c_double)]),
     "gemm_tile_raster": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64),
                                 ctypes.POINTER(_i64)]),
+    "gemm_sgemm_config": (_int, [_int, _vp]),
 }
+
+class SgemmConfig(ctypes.Structure):
+    """gemm_sgemm_config_t of include/gemm_gb300.h."""
+    _fields_ = [("name", ctypes.c_char)] + [(f, ctypes.c_int) for f in (
+        "bm", "bn", "bk", "tm", "tn", "stages", "threads", "ctas_per_sm", "row_pad", "smem_bytes")]
+
 
 _lock = threading.Lock()
 _lib = None

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "gemm_internal.h"
+#include "sgemm_kernel.cuh"
 
 namespace gemm {
 
@@ -319,6 +320,23 @@ const char *gemm_status_string(gemm_status_t status)
 int gemm_version(void) { return 100; }
 
 uint64_t gemm_kernel_launches(void) { return gemm::launches_so_far(); }
+
+gemm_status_t gemm_sgemm_config(int index, gemm_sgemm_config_t *out)
+{
+    if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+    auto fill = [out](char name, auto cfg) {
+        using C = decltype(cfg);
+        *out = gemm_sgemm_config_t{name, C::BM, C::BN, C::BK, C::TM, C::TN, C::STAGES, sg::kThreads,
+                                   C::MIN_BLOCKS, C::PAD, C::SMEM_BYTES};
+        return GEMM_OK;
+    };
+    switch (index) {
+    case 0: return fill('L', sg::CfgL{});
+    case 1: return fill('M', sg::CfgM{});
+    case 2: return fill('S', sg::CfgS{});
+    default: return GEMM_ERR_INVALID_VALUE;
+    }
+}
 
 gemm_status_t gemm_tile_raster(int64_t t, int64_t tiles_m, int64_t tiles_n, int log_group,
                                int64_t *tile_m, int64_t *tile_n)

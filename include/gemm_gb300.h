@@ -252,6 +252,23 @@ GEMM_API uint64_t gemm_kernel_launches(void);
 GEMM_API gemm_status_t gemm_measure_fp32_fma_peak(void *stream, double *tflops);
 
 /*
+ * The tile configurations of the strict-FP32 path (a host function: needs no GPU), for
+ * tools and tests.  Configuration `index` (0, 1, ... in the order the planner considers
+ * them) is written to *out: its one-letter name, block tile BM x BN, K slice BK, thread tile
+ * TM x TN, ring stages, threads per CTA, the CTAs per SM it is compiled for, the padding of
+ * each [k][x] stage row in floats (0: XOR-swizzled rows), and its dynamic shared memory,
+ * STAGES * BK * (BM + BN + 2 * pad) * 4 bytes -- the footprint arithmetic of the ssxxe.cn
+ * GEMM page, section "2.1 矩阵分块利用Shared Memory", BK * (BM + BN) * 4 bytes per stage,
+ * plus the padding.  Returns GEMM_ERR_INVALID_VALUE for an index past the last
+ * configuration or a NULL output.
+ */
+typedef struct {
+    char name;
+    int bm, bn, bk, tm, tn, stages, threads, ctas_per_sm, row_pad, smem_bytes;
+} gemm_sgemm_config_t;
+GEMM_API gemm_status_t gemm_sgemm_config(int index, gemm_sgemm_config_t *out);
+
+/*
  * Tile raster used by the kernels (a host function: needs no GPU).  It maps the t-th tile
  * of a tiles_m x tiles_n grid of output tiles to (tile_m, tile_n) so that consecutive
  * tiles sweep a group of 2^log_group tile rows column by column, which keeps the operand

@@ -129,3 +129,27 @@ def test_binding_host_entry_refuses_wrong_types(lib):
 
 def test_fma_peak_probe_rejects_a_null_output_without_a_device(lib):
     assert lib.gemm_measure_fp32_fma_peak(None, ctypes.POINTER(ctypes.c_double)()) == 1
+
+
+def test_config_table_follows_the_pages_footprint_arithmetic(lib):
+    # The pages' worked example (ssxxe.cn GEMM page, section 2.1): a 128 x 128 block tile with
+    # BK = 8 holds BK * (BM + BN) * 4 = 8192 bytes of fp32 tiles and does 32 flop per byte
+    # loaded.  The library's configurations account their shared memory the same way per
+    # ring stage (plus one 16-byte chunk of padding per padded [k][x] row), fit the CTAs per
+    # SM they are compiled for, and the 128 x 128 one has the example's intensity.
+    d = golden_io.read("smem_footprint.txt")
+    BM, BN, BK = (golden_io.scalar(d, k) for k in ("BM", "BN", "BK"))
+    assert BK * (BM + BN) * 4 == golden_io.scalar(d, "smem_bytes")
+    assert 2 * BM * BN * BK / ((BM + BN) * BK * 4) == golden_io.scalar(d, "flop_per_byte")
+    configs = g.gemm_sgemm_configs()
+    assert [c["name"] for c in configs] == ["L", "M", "S"]
+    for c in configs:
+        assert c["smem_bytes"] == c["stages"] * c["bk"] * (c["bm"] + c["bn"] + 2 * c["row_pad"]) * 4
+        assert c["threads"] == (c["bm"] // c["tm"]) * (c["bn"] // c["tn"])
+        assert c["row_pad"] in (0, 4)
+        assert c["ctas_per_sm"] * (c["smem_bytes"] + 1024) <= 228 * 1024  # 228 KB per SM
+    L = [c for c in configs if (c["bm"], c["bn"]) == (BM, BN)][0]
+    assert 2 * L["bm"] * L["bn"] * L["bk"] / ((L["bm"] + L["bn"]) * L["bk"] * 4) == \
+        golden_io.scalar(d, "flop_per_byte")
+    c = g.load().gemm_sgemm_config(len(configs), ctypes.byref(_lib.SgemmConfig()))
+    assert c == 1  # past the last configuration
