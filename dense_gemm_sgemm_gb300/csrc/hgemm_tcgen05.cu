@@ -4,21 +4,31 @@
 // (copecc.github.io "GEMM" page, sections "核心问题与运算特征" and "Batched 执行与混合精度";
 // dandandamowang.xyz "GEMM优化（二）": fp16 inputs, fp32 accumulator).  The pages reach the
 // tensor cores through WMMA fragments on one warp at a time; on Blackwell the same
-// contraction is issued by ONE thread per CTA as tcgen05.mma, with operands read straight
-// from shared memory through matrix descriptors and the fp32 accumulator kept in tensor
-// memory (TMEM).  The kernel is persistent and warp-specialised:
+// contraction is issued by ONE thread as tcgen05.mma, with operands read straight from
+// shared memory through matrix descriptors and the fp32 accumulator kept in tensor memory
+// (TMEM).  The kernel is persistent and warp-specialised:
 //
 //   warp 0      TMA producer: one elected lane streams BK-wide K slices of the A and B
-//               tiles into a STAGES-deep shared-memory ring (cp.async.bulk.tensor with
-//               128-byte swizzle; the pages' cp.async double buffer of the "v4" section,
-//               moved to the tensor-memory-access unit and deepened);
+//               tiles into a shared-memory ring (cp.async.bulk.tensor with 128-byte
+//               swizzle; the pages' cp.async double buffer of the "v4" section, moved to
+//               the tensor-memory-access unit and deepened);
 //   warp 1      MMA issuer and TMEM owner: allocates 512 TMEM columns (two 128 x 256 fp32
-//               accumulators), issues 4 tcgen05.mma (M=128, N=256, K=16) per slice and
-//               returns each slice to the producer with tcgen05.commit;
+//               accumulators), issues 4 tcgen05.mma (K=16) per slice and returns each
+//               slice to the producer with tcgen05.commit;
 //   warps 2-5   epilogue: tcgen05.ld the finished accumulator (one TMEM lane = one row of
 //               the tile), pass each 32 x 32 piece through a shared staging tile so that
 //               C = alpha * acc + beta * C is read and written in 128-byte row segments,
 //               while warp 1 already accumulates the next tile into the other buffer.
+//
+// Two forms.  PAIR = true (any problem of at least two 128-row tile rows): clusters of two
+// CTAs on neighbouring SMs compute a 256 x 256 tile with tcgen05.mma.cta_group::2 (M=256,
+// N=256).  Each CTA loads only its own 128 rows of A and its own 128 columns of B, a
+// 32 KB stage per K slice, and the MMA reads the B halves of both CTAs: per SM this moves
+// two thirds of the bytes of a one-CTA 128 x 256 tile through L2 and shared memory, and
+// lets 6 stages fit.  Only the first CTA of the pair (rank 0) issues MMAs; both CTAs' TMA
+// loads complete on its "full" barriers, and its commits release the "empty" barriers of
+// both CTAs.  PAIR = false: one CTA computes a 128 x 256 tile with cta_group::1 MMAs from
+// a 4-stage ring of 48 KB stages.
 //
 // The last, partial wave of tiles is split so that more SMs share it: into K halves whose
 // fp32 partial sums are exchanged (each half finishes half of the tile's columns), or into
@@ -48,17 +58,27 @@ __device__ unsigned int g_device_status = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;  // BM: rows per CTA
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kAccCols = BN;        // fp32 columns per accumulator
 constexpr int kTmemCols = 2 * BN;   // two accumulators
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int EPI_BYTES = 4 * 32 * 32 * 4;  // a 32 x 32 fp32 staging tile per epilogue warp
 constexpr int kBarBytes = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
 constexpr int kLogGroup = 3;
+
+// Ring geometry of the two forms: a CTA of a pair holds half of the B columns.
+template <bool PAIR>
+struct Ring {
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kBStageBytes = (PAIR ? BN / 2 : BN) * BK * 2;  // 16 KB or 32 KB
+    static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
+};
+static_assert(Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024,
+              "one CTA per SM within the 227 KB opt-in limit");
+constexpr int kMaxSmemBytes =
+    Ring<true>::kSmemBytes > Ring<false>::kSmemBytes ? Ring<true>::kSmemBytes : Ring<false>::kSmemBytes;
 
 struct HgemmParams {
     int64_t M, N, K;
@@ -215,16 +235,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Multicast load: the box lands at the same shared-memory offset in every CTA of the cluster
-// named in cta_mask, and each of them gets the complete_tx on its barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t c0, int32_t c1, int32_t c2, uint16_t cta_mask)
+// The same copy issued by a CTA of a two-CTA pair whose completion is counted on an
+// mbarrier that may sit in either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2)
 {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of
+// this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its shared::cluster address,
+// which may be in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -261,33 +297,67 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], one CTA, fp16 inputs, fp32 accumulate.
+// D[tmem] (+)= A[smem desc] * B[smem desc], fp16/bf16 inputs, fp32 accumulate.  PAIR:
+// issued by rank 0 of a CTA pair for both CTAs (M = 256: each CTA's descriptors name its
+// own 128 rows of A and its own half of the B columns at the same shared-memory offsets;
+// each CTA's TMEM receives its own 128 rows of D).
+template <bool PAIR>
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (PAIR) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
-// Arrives on `bar` once every tcgen05.mma issued so far by this thread has completed.
+// Arrives on the mbarrier at shared::cluster address `bar` (this CTA's or, for a pair, the
+// peer's) once every tcgen05.mma issued so far by this thread has completed.
+template <bool PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
 }
 
-// The same, arriving on the barrier at offset `bar` in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask)
+// TMEM allocation by one whole warp; for a pair, one warp of each CTA calls it together and
+// both receive the same columns.
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t cols)
 {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t cols)
+{
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -327,34 +397,35 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-9 and
 // 10-12 = 0), A/B major-ness in bits 15/16 (0 = K-major, 1 = MN-major), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn, int n = BN)
+// 17-22, M >> 4 in bits 24-28 (M = 128 for one CTA, 256 for a pair).
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn, int n, int m)
 {
     return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
-           (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+           (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ the kernel
-// MC = false: one CTA per tile.  MC = true: clusters of two CTAs along M share the B tile --
-// each loads its own A and half of B, multicasting that half to both CTAs, so each SM's
-// tensor-memory-access unit moves 32 KB instead of 48 KB per K slice.  Units then count
-// tile pairs: the CTA of cluster rank r computes tile row 2 * pair_row + r.
-template <int A_MN, int B_MN, bool MC>
+// PAIR = false: one CTA per 128 x 256 tile.  PAIR = true: units count tile pairs along M;
+// the CTA of cluster rank r computes tile row 2 * pair_row + r, and rank 0 issues the
+// pair's MMAs.
+template <int A_MN, int B_MN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_b_half,
                      const __grid_constant__ CUtensorMap map_b_quarter, const HgemmParams p)
 {
+    using R = Ring<PAIR>;
+    constexpr int STAGES = R::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
 
-    const uint32_t sA = base;                          // STAGES x 16 KB
-    const uint32_t sB = base + STAGES * A_STAGE_BYTES; // STAGES x 32 KB
-    float4 *epi_tiles = reinterpret_cast<float4 *>(smem + STAGES * STAGE_BYTES);
-    uint8_t *bar_area = smem + STAGES * STAGE_BYTES + EPI_BYTES;
+    const uint32_t sA = base;                                // STAGES x 16 KB
+    const uint32_t sB = base + STAGES * A_STAGE_BYTES;       // STAGES x (16 or 32) KB
+    float4 *epi_tiles = reinterpret_cast<float4 *>(smem + STAGES * R::kStageBytes);
+    uint8_t *bar_area = smem + STAGES * R::kStageBytes + EPI_BYTES;
     const uint32_t bar0 = smem_u32(bar_area);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -363,25 +434,26 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * STAGES + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * STAGES + 5) + 4);
+    static_assert(8 * (2 * STAGES + 5) + 8 <= kBarBytes, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Unit schedule: CTAs (or clusters) stride over the units; the raster runs over tiles
-    // (or tile pairs along M).
-    const int rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
-    const int64_t unit0 = MC ? int64_t(cluster_id_x()) : int64_t(blockIdx.x);
-    const int64_t ustride = MC ? int64_t(cluster_count_x()) : int64_t(gridDim.x);
-    const int64_t rows_r = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
-    constexpr uint16_t kPair = 0x3;
+    // Unit schedule: CTAs (or pairs) stride over the units; the raster runs over tiles (or
+    // tile pairs along M).
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int64_t unit0 = PAIR ? int64_t(cluster_id_x()) : int64_t(blockIdx.x);
+    const int64_t ustride = PAIR ? int64_t(cluster_count_x()) : int64_t(gridDim.x);
+    const int64_t rows_r = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
+    constexpr int kEpiArrivals = PAIR ? 8 : 4;  // one per epilogue warp of every CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), MC ? 2 : 1);  // MC: both CTAs' MMAs release a slot
+            mbar_init(full_bar(s), 1);   // the arming arrival of rank 0's producer
+            mbar_init(empty_bar(s), 1);  // the MMA issuer's commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4 * 32);
+            mbar_init(acce_bar(b), kEpiArrivals);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -389,18 +461,16 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
         tma_prefetch_desc(&map_b_half);
-        if (MC) tma_prefetch_desc(&map_b_quarter);
+        tma_prefetch_desc(&map_b_quarter);
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(const_cast<uint32_t *>(tmem_slot))),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    // A pair allocates TMEM together, so the peer must be running; its barriers must also
+    // exist before the other CTA's copies, commits and arrivals reach them.
+    if (PAIR) cluster_sync();
+    if (warp == 1) tmem_alloc<PAIR>(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
     tc_fence_before();
-    __syncthreads();
-    if (MC) cluster_sync();  // the peer's barriers exist before any multicast targets them
+    // a pair: both CTAs hold their columns before rank 0's MMAs can write them
+    if (PAIR) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -408,7 +478,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (each CTA fills its own ring)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per stage: a fill was issued / its parity
@@ -420,20 +490,23 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 int64_t tm, tn;
                 const int64_t bt = t / p.per_batch;
                 raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
-                if (MC) tm = 2 * tm + rank;
+                if (PAIR) tm = 2 * tm + rank;
                 const int32_t ba = p.a_batched ? static_cast<int32_t>(bt) : 0;
                 const int32_t bb = p.b_batched ? static_cast<int32_t>(bt) : 0;
                 const int32_t m0 = static_cast<int32_t>(tm * BM);
-                const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off;
-                const uint32_t bytes = A_STAGE_BYTES + uint32_t(width) * BK * 2;
+                // a pair's CTA loads B columns [n0, n0 + bw) of the unit
+                const int bw = PAIR ? width / 2 : width;
+                const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off + (PAIR ? int32_t(rank) * bw : 0);
+                // bytes that complete a slice on the (rank 0) full barrier: both CTAs' for a pair
+                const uint32_t bytes = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + uint32_t(bw) * BK * 2);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
                         raise_abort(abort_flag);
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = full_bar(stage);
-                    mbar_expect_tx(fb, bytes);
+                    const uint32_t fb = PAIR ? map_to_rank(full_bar(stage), 0) : full_bar(stage);
+                    if (rank == 0) mbar_expect_tx(full_bar(stage), bytes);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     const bool stall = kb == x.kb0 && ((p.inject_stall == 1 && u == unit0) ||
@@ -441,32 +514,21 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     if (!stall) {
                         const int32_t k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
-                        const uint32_t b_dst = sB + stage * B_STAGE_BYTES;
+                        const uint32_t b_dst = sB + stage * R::kBStageBytes;
+                        auto load = [&](uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
+                            if (PAIR) tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+                            else tma_load_3d(dst, map, fb, c0, c1, c2);
+                        };
                         if (A_MN) {  // A stored K x M: two 64 (m) x 64 (k) boxes
-                            tma_load_3d(a_dst, &map_a, fb, m0, k0, ba);
-                            tma_load_3d(a_dst + 8192, &map_a, fb, m0 + 64, k0, ba);
+                            load(a_dst, &map_a, m0, k0, ba);
+                            load(a_dst + 8192, &map_a, m0 + 64, k0, ba);
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
-                            tma_load_3d(a_dst, &map_a, fb, k0, m0, ba);
+                            load(a_dst, &map_a, k0, m0, ba);
                         }
-                        if (MC) {
-                            // This CTA's half of the unit's B columns, multicast to both CTAs.
-                            const int half = width / 2;
-                            const int32_t nb = n0 + rank * half;
-                            const uint32_t bd = b_dst + uint32_t(rank) * uint32_t(half) * 128u;
-                            if (B_MN) {
-                                for (int j = 0; j < half / 64; ++j)
-                                    tma_load_3d_mc(bd + 8192 * j, &map_b, fb, nb + 64 * j, k0, bb, kPair);
-                            } else {
-                                tma_load_3d_mc(bd, half == BN / 2 ? &map_b_half : &map_b_quarter, fb, k0, nb, bb,
-                                               kPair);
-                            }
-                        } else if (B_MN) {  // B stored K x N: width / 64 boxes of 64 (n) x 64 (k)
-                            for (int j = 0; j < width / 64; ++j)
-                                tma_load_3d(b_dst + 8192 * j, &map_b, fb, n0 + 64 * j, k0, bb);
-                        } else if (width == BN) {  // B stored N x K: one 64 (k) x 256 (n) box
-                            tma_load_3d(b_dst, &map_b, fb, k0, n0, bb);
-                        } else {     // half-width unit: one 64 (k) x 128 (n) box
-                            tma_load_3d(b_dst, &map_b_half, fb, k0, n0, bb);
+                        if (B_MN) {  // B stored K x N: bw / 64 boxes of 64 (n) x 64 (k)
+                            for (int j = 0; j < bw / 64; ++j) load(b_dst + 8192 * j, &map_b, n0 + 64 * j, k0, bb);
+                        } else {     // B stored N x K: one 64 (k) x bw (n) box
+                            load(b_dst, bw == BN ? &map_b : bw == BN / 2 ? &map_b_half : &map_b_quarter, k0, n0, bb);
                         }
                     } else {
                         filled &= ~(1u << stage);  // nothing in flight on this slot
@@ -475,15 +537,24 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 }
             }
             if (!ok) {
-                // Let the copies already issued land before the CTA's shared memory goes away.
-                for (int s = 0; s < STAGES; ++s)
-                    if ((filled >> s) & 1u) {
-                        const volatile int no_abort = 0;
-                        mbar_wait(full_bar(s), (fill_parity >> s) & 1u, &no_abort, 100000000ull);
+                if (PAIR) {
+                    // This CTA's copies complete on rank 0's barriers, which it cannot wait on:
+                    // give the copies already issued time to land before its shared memory
+                    // may go away (a TMA load of one stage takes microseconds).
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 2000000ull) {
                     }
-            } else if (MC) {
-                // Wait for the last release of every slot by both CTAs' MMAs, so that no
-                // arrival from the peer is still on its way when this CTA exits.
+                } else {
+                    // Let the copies already issued land before the CTA's shared memory goes away.
+                    for (int s = 0; s < STAGES; ++s)
+                        if ((filled >> s) & 1u) {
+                            const volatile int no_abort = 0;
+                            mbar_wait(full_bar(s), (fill_parity >> s) & 1u, &no_abort, 100000000ull);
+                        }
+                }
+            } else if (PAIR) {
+                // Wait for the last release of every slot, so that no commit from rank 0 is
+                // still on its way to this CTA's barriers when it exits.
                 for (int i = 0; i < STAGES; ++i) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
                         raise_abort(abort_flag);
@@ -494,11 +565,12 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (rank 0 of a pair issues for both CTAs)
+            constexpr int kM = PAIR ? 2 * BM : BM;
             const uint32_t fmt = (p.ab_format << 7) | (p.ab_format << 10);  // A and B input type
-            const uint32_t idesc_full = make_idesc(A_MN, B_MN, BN) | fmt;
-            const uint32_t idesc_half = make_idesc(A_MN, B_MN, BN / 2) | fmt;
+            const uint32_t idesc_full = make_idesc(A_MN, B_MN, BN, kM) | fmt;
+            const uint32_t idesc_half = make_idesc(A_MN, B_MN, BN / 2, kM) | fmt;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -521,7 +593,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     }
                     tc_fence_after();
                     const uint32_t a_tile = sA + stage * A_STAGE_BYTES;
-                    const uint32_t b_tile = sB + stage * B_STAGE_BYTES;
+                    const uint32_t b_tile = sB + stage * R::kBStageBytes;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // K-major: step 32 bytes along the swizzled 128-byte row.
@@ -530,21 +602,22 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                                                  : smem_desc(a_tile + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc(b_tile + k * 2048, 8192, 1024)
                                                  : smem_desc(b_tile + k * 32, 16, 1024);
-                        umma_f16(d_tmem, ad, bd, idesc, (kb > x.kb0 || k > 0) ? 1u : 0u);
+                        umma_f16<PAIR>(d_tmem, ad, bd, idesc, (kb > x.kb0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
-                    // slot free once these MMAs have read it (MC: in both CTAs' counts)
-                    if (MC) umma_commit_mc(empty_bar(stage), kPair);
-                    else umma_commit(empty_bar(stage));
+                    // the slot is free once these MMAs have read it (a pair: in both CTAs)
+                    umma_commit<PAIR>(empty_bar(stage));
+                    if (PAIR) umma_commit<PAIR>(map_to_rank(empty_bar(stage), 1));  // the peer's slot
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(accf_bar(acc));  // accumulator complete
+                umma_commit<PAIR>(accf_bar(acc));  // accumulator complete
+                if (PAIR) umma_commit<PAIR>(map_to_rank(accf_bar(acc), 1));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok && issued) {
                 // Wait for the MMAs in flight before TMEM is released.
-                umma_commit(drain_bar);
+                umma_commit<PAIR>(drain_bar);
                 const volatile int no_abort = 0;
                 mbar_wait(drain_bar, 0, &no_abort, 100000000ull);
             }
@@ -562,7 +635,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             int64_t tm, tn;
             const int64_t bt = t / p.per_batch;
             raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
-            if (MC) tm = 2 * tm + rank;
+            if (PAIR) tm = 2 * tm + rank;
             // The four epilogue warps leave together or not at all: a K-half unit below
             // synchronises them, so none may have given up on a unit the others continue.
             const bool got = mbar_wait(accf_bar(acc), acc_phase, abort_flag, tmo);
@@ -645,7 +718,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 // capacity, so the wait ends unless a fault aborts the kernel.
                 const int e = threadIdx.x - 64;
                 const int h = x.khalf;
-                const int64_t slot = MC ? 2 * x.split_slot + rank : x.split_slot;
+                const int64_t slot = PAIR ? 2 * x.split_slot + rank : x.split_slot;
                 constexpr int QH = BN / 8;  // float4 per row of a half tile
                 float4 *mine = reinterpret_cast<float4 *>(p.ws) + (slot * 2 + h) * (QH * 128) + e;
                 const float4 *other = reinterpret_cast<const float4 *>(p.ws) + (slot * 2 + (h ^ 1)) * (QH * 128) + e;
@@ -683,7 +756,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 if (epilogue_any(failed)) {
                     raise_abort(abort_flag);
                 } else {
-                    static_assert(QH * 128 * 16 <= STAGES * STAGE_BYTES, "the ring holds a partial half tile");
+                    static_assert(QH * 128 * 16 <= STAGES * R::kStageBytes, "the ring holds a partial half tile");
                     const uint32_t stage_dst = sA + uint32_t(e) * 16u;
 #pragma unroll 8
                     for (int q = 0; q < QH; ++q)
@@ -707,8 +780,13 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                     }
                 }
             }
+            // accumulator may be overwritten: one arrival per warp on the issuer's barrier
             tc_fence_before();
-            mbar_arrive(acce_bar(acc));  // accumulator may be overwritten
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR) mbar_arrive_cluster(map_to_rank(acce_bar(acc), 0));
+                else mbar_arrive(acce_bar(acc));
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
@@ -716,12 +794,9 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (MC) cluster_sync();  // neither CTA leaves while the other may still signal it
+    if (PAIR) cluster_sync();  // neither CTA leaves or frees TMEM while the other may still use it
     tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                     : "memory");
-    }
+    if (warp == 1) tmem_free<PAIR>(tmem_base, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -767,7 +842,7 @@ struct Maps {
     CUtensorMap a, b, b_half, b_quarter;
 };
 
-// Largest number of two-CTA clusters of this kernel that can be resident at once (0: none).
+// Largest number of two-CTA clusters of the pair kernel that can be resident at once (0: none).
 template <int A_MN, int B_MN>
 int max_pair_clusters(int dev_id)
 {
@@ -778,7 +853,7 @@ int max_pair_clusters(int dev_id)
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -796,47 +871,48 @@ int max_pair_clusters(int dev_id)
     return n;
 }
 
-template <int A_MN, int B_MN, bool MC>
+template <int A_MN, int B_MN, bool PAIR>
 cudaError_t set_smem_attr(int dev_id)
 {
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = uint64_t(1) << (dev_id & 63);
     if (attr_set.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, MC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<PAIR>::kSmemBytes);
     if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_release);
     return e;
 }
 
-// Plans the unit schedule and launches.  With clusters, units are tile pairs along M.
+// Plans the unit schedule and launches.  With pairs, units are tile pairs along M.
 template <int A_MN, int B_MN>
 cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaStream_t stream)
 {
-    const char *no_mc = std::getenv("GEMM_GB300_HGEMM_NO_MULTICAST");
+    // GEMM_GB300_HGEMM_PAIR=0: one CTA per tile even where pairs would be used
+    const char *pair_env = std::getenv("GEMM_GB300_HGEMM_PAIR");
     // GEMM_GB300_HGEMM_TAIL: "0" no tail split, "n" N halves, otherwise the rule below
     const char *tail_env = std::getenv("GEMM_GB300_HGEMM_TAIL");
     const char tail_want = tail_env && tail_env[0] ? tail_env[0] : 'a';
-    bool mc = p.tiles_m >= 2 && !(no_mc && no_mc[0] == '1');
+    bool pair = p.tiles_m >= 2 && !(pair_env && pair_env[0] == '0');
     int max_clusters = 0;
-    if (mc) {
+    if (pair) {
         if (set_smem_attr<A_MN, B_MN, true>(dev.device) != cudaSuccess) return cudaGetLastError();
         max_clusters = max_pair_clusters<A_MN, B_MN>(dev.device);
-        mc = max_clusters > 0;
+        pair = max_clusters > 0;
     }
     // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
     // half of the workers idle, its tiles are split in two units each: K halves when there
     // are at least 8 K slices and the stream's workspace holds the partial tiles, else N
     // halves.
-    p.per_batch = mc ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
+    p.per_batch = pair ? ((p.tiles_m + 1) / 2) * p.tiles_n : p.num_tiles;
     const int64_t work = p.per_batch * p.batch;
-    const int64_t workers_max = mc ? max_clusters : dev.num_sms;
+    const int64_t workers_max = pair ? max_clusters : dev.num_sms;
     const int64_t workers = work < workers_max ? work : workers_max;
     p.full_tiles = work;
     p.num_units = work;
     p.tail_mode = kTailNone;
     const int64_t full = (work / workers) * workers, tail = work - full;
     if (tail > 0 && 2 * tail <= workers && tail_want != '0') {
-        const int64_t split_tiles = tail * (mc ? 2 : 1);  // CTA tiles of the split units
+        const int64_t split_tiles = tail * (pair ? 2 : 1);  // CTA tiles of the split units
         StreamWorkspace w;
         if (tail_want != 'n' && p.num_kb >= 8 && split_tiles <= int64_t(kWorkspaceCounters) &&
             size_t(split_tiles) * 2 * BM * BN * sizeof(float) <= kWorkspaceBytes &&
@@ -850,11 +926,12 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         p.full_tiles = full;
         p.num_units = full + 2 * tail;
     }
-    if (!mc) {
+    if (!pair) {
         cudaError_t e = set_smem_attr<A_MN, B_MN, false>(dev.device);
         if (e != cudaSuccess) return e;
-        hgemm_tcgen05_kernel<A_MN, B_MN, false><<<static_cast<unsigned>(workers), kThreads, SMEM_BYTES, stream>>>(
-            m.a, m.b, m.b_half, m.b_quarter, p);
+        hgemm_tcgen05_kernel<A_MN, B_MN, false>
+            <<<static_cast<unsigned>(workers), kThreads, Ring<false>::kSmemBytes, stream>>>(m.a, m.b, m.b_half,
+                                                                                           m.b_quarter, p);
         const cudaError_t le = cudaGetLastError();
         if (le == cudaSuccess) count_launches();
         return le;
@@ -862,7 +939,7 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * workers), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -884,7 +961,7 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
                            const uint16_t *B, int64_t ldb, int64_t strideB, float beta, float *C,
                            int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream)
 {
-    if (dev.smem_optin < size_t(SMEM_BYTES)) return GEMM_ERR_NO_DEVICE;
+    if (dev.smem_optin < size_t(kMaxSmemBytes)) return GEMM_ERR_NO_DEVICE;
     const int a_mn = opA == GEMM_OP_T;  // A stored K x M
     const int b_mn = opB == GEMM_OP_N;  // B stored K x N
     const int bf = dtype == kInBf16;

@@ -45,6 +45,25 @@ def test_integer_bit_exact(opA, opB):
     parity.check_full(w, inputs, dev["C"], integer=True)
 
 
+@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_pair_and_single_cta_paths_full_oracle(opA, opB, dtype, monkeypatch):
+    # Two-CTA tiles (tcgen05.mma.cta_group::2, each CTA holding its own A rows and half of the
+    # B columns) and one-CTA tiles on the same problem: an odd number of 128-row tile rows
+    # (the last pair has no second row), ragged N and K, several tiles per CTA.
+    M, N, K = 1408 + 77, 2048 + 40, 904
+    w0 = workloads.Workload("probe", dtype, M, N, K, opA, opB)
+    pad = (_pad8(w0.a_shape[1]), _pad8(w0.b_shape[1]), 0)
+    w = workloads.Workload(f"hgemm_pairs_{dtype}_{opA}{opB}", dtype, M, N, K, opA, opB,
+                           alpha=1.25, beta=-0.5, seed=31, pad=pad)
+    inputs = workloads.make_inputs(w)
+    for pair in (True, False):
+        if not pair:
+            monkeypatch.setenv("GEMM_GB300_HGEMM_PAIR", "0")
+        _, dev = _run(w, inputs)
+        parity.check_full(w, inputs, dev["C"])
+
+
 def test_persistent_tiles_and_double_buffered_accumulator():
     # 18 x 10 = 180 tiles of 128 x 256: several CTAs run two tiles through both TMEM buffers
     w = workloads.Workload("hgemm_2304x2560x192", "f16", 2304, 2560, 192, alpha=0.75, beta=0.5,
@@ -143,19 +162,19 @@ def test_beta_zero_ignores_nan():
 TAIL_MODES = ["auto", "n"]
 
 
-def _tail_env(monkeypatch, mode, multicast=True):
+def _tail_env(monkeypatch, mode, pair=True):
     if mode != "auto":
         monkeypatch.setenv("GEMM_GB300_HGEMM_TAIL", mode)
-    if not multicast:
-        monkeypatch.setenv("GEMM_GB300_HGEMM_NO_MULTICAST", "1")
+    if not pair:
+        monkeypatch.setenv("GEMM_GB300_HGEMM_PAIR", "0")
 
 
-@pytest.mark.parametrize("multicast", [True, False])
+@pytest.mark.parametrize("pair", [True, False])
 @pytest.mark.parametrize("mode", TAIL_MODES)
-def test_tail_wave_split_units_full_oracle(mode, multicast, monkeypatch):
-    # 18 x 10 = 180 tiles of 128 x 256 (90 pairs with two-CTA clusters): the tiles of the last
-    # wave run as two units each on different SMs.
-    _tail_env(monkeypatch, mode, multicast)
+def test_tail_wave_split_units_full_oracle(mode, pair, monkeypatch):
+    # 18 x 10 = 180 tiles of 128 x 256 (90 tile pairs for the two-CTA MMA): the tiles of the
+    # last wave run as two units each on different SMs.
+    _tail_env(monkeypatch, mode, pair)
     w = workloads.Workload("hgemm_tail_2300x2560x512", "f16", 2300, 2560, 512, alpha=0.75,
                            beta=0.5, seed=12, pad=(0, 0, 3))
     inputs, dev = _run(w)
