@@ -136,8 +136,8 @@ def gemm_sgemm_f32_noalloc(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ld
     """gemm_sgemm_f32 for callers that must not allocate device memory during the call.
 
     The split-K scratch is a fixed 16 MiB + 16 KiB device array owned by the library (no
-    cudaMalloc ever); problems with more than 1024 tiles of 64 x 64 are refused
-    (GEMM_ERR_UNSUPPORTED), and calls that overlap on the GPU must not share the array.
+    cudaMalloc ever); K is split only as far as the array holds the partial tiles (problems
+    too large for that run unsplit), and calls that overlap on the GPU must not share the array.
     """
     import torch
 

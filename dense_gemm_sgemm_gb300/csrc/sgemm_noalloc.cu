@@ -9,7 +9,8 @@
 // point never calls cudaMalloc, cudaFree or any other allocating routine.
 //
 // The price: the scratch array below exists on every GPU that loads this library, for as
-// long as the process lives, and bounds the problems this entry point accepts.
+// long as the process lives, and bounds how far a problem's K is split (a problem too large
+// to split within it runs unsplit, which needs no scratch).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -92,24 +93,27 @@ extern "C" GEMM_API gemm_status_t gemm_sgemm_f32_noalloc(gemm_op_t opA, gemm_op_
         return GEMM_ERR_MISALIGNED;
 
     // Grid of 64 x 64 tiles and K splits: enough splits to fill one wave of three CTAs per
-    // SM, at most 16, at least two 16-wide K slices each, within the scratch array.
+    // SM, at most 16, at least two 16-wide K slices each.  A split count above one needs an
+    // arrival counter per tile and a partial tile per split and tile in the scratch array;
+    // where they would not fit, fewer splits are taken, down to one, which uses no scratch.
     const int64_t tiles_m = (M + CfgS::BM - 1) / CfgS::BM, tiles_n = (N + CfgS::BN - 1) / CfgS::BN;
     const int64_t tiles = tiles_m * tiles_n;
     const int64_t KT = (K + CfgS::BK - 1) / CfgS::BK;
-    if (tiles > kNoallocCounters || size_t(tiles) * kTileBytes > kNoallocPartialBytes)
-        return GEMM_ERR_UNSUPPORTED;  // the partial tiles would not fit the scratch array
     DeviceInfo dev;
     if (!current_device(dev) || dev.cc_major != 10 || dev.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
     const int64_t target = int64_t(dev.num_sms) * CfgS::MIN_BLOCKS;
     int64_t S = (target + tiles / 2) / tiles;
     S = S < 1 ? 1 : (S > 16 ? 16 : S);
-    while (S > 1 && (KT / S < 2 || size_t(tiles) * S * kTileBytes > kNoallocPartialBytes)) --S;
+    while (S > 1 && (KT / S < 2 || tiles > kNoallocCounters ||
+                     size_t(tiles) * S * kTileBytes > kNoallocPartialBytes))
+        --S;
 
+    // The address lookup is the per-device set-up of the first call, split or not.
     unsigned char *scratch = nullptr;
     if (!scratch_address(dev.device, &scratch)) return GEMM_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents; the arrival counters must start at zero.
-    if (cudaMemsetAsync(scratch, 0, size_t(tiles) * sizeof(unsigned int), st) != cudaSuccess)
+    if (S > 1 && cudaMemsetAsync(scratch, 0, size_t(tiles) * sizeof(unsigned int), st) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
 
     SgemmParams p{};

@@ -203,8 +203,10 @@ GEMM_API gemm_status_t gemm_bgemm_bf16f32_host(gemm_op_t opA, gemm_op_t opB, int
  * holds on every GPU that loads it, until the process exits; the call itself never calls
  * cudaMalloc, cudaFree or any allocating routine.
  *
- * Limit: ceil(M/64) * ceil(N/64) <= 1024 (the partial tiles of one split must fit 16 MiB);
- * larger problems return GEMM_ERR_UNSUPPORTED without launching anything.
+ * The K split count S is reduced until the split's scratch fits the array: at most 4096
+ * tiles of 64 x 64 and tiles * S <= 1024 partial tiles.  S = 1 uses no scratch, so problems
+ * too large to split still run (unsplit).
+ * Limits: M, N, K < 2^31; larger sizes return GEMM_ERR_UNSUPPORTED without launching anything.
  * The first call on a device looks up the device address of the scratch array (with that
  * device current); make that first call before capturing the stream into a graph.
  * Every call shares the one array, whose contents persist between calls: the call clears

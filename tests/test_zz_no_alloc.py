@@ -3,9 +3,10 @@
 Some callers cannot let a library call cudaMalloc while they run -- a framework whose own
 allocator owns the device memory, or a latency-critical path where an allocation could
 block, synchronise the device or fail.  This entry point keeps its split-K scratch in a
-fixed device array inside the library.  These tests call it through the C ABI and compare
-it with gemm_sgemm_f32 on the same inputs, twice in a row (the second call reuses the
-scratch the first one left behind).  The file is named to be collected last.
+fixed device array inside the library.  These tests call it through the C ABI, twice in a
+row (the second call reuses the scratch the first one left behind), and check each result
+against the CPU oracle and against gemm_sgemm_f32 on the same inputs.  The file is named to
+be collected last.
 """
 import numpy as np
 import pytest
@@ -23,6 +24,9 @@ CASES = [
     workloads.sgemm_256(),                          # 16 tiles, split 8
     workloads.Workload("noalloc_opT_pad", "f32", 300, 200, 700, "T", "T", alpha=0.5, beta=2.0,
                        seed=31, pad=(3, 1, 2)),    # unaligned lds, both operands transposed
+    # 4096 tiles of 64 x 64: too many to split within the scratch array, so K is not split
+    workloads.Workload("noalloc_unsplit_4096x4096x96", "f32", 4096, 4096, 96, alpha=1.0,
+                       beta=-1.0, seed=32),
 ]
 
 
@@ -35,17 +39,18 @@ def _call(fn, w, dev, c_init):
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_matches_gemm_sgemm_f32_on_two_calls_in_a_row(w):
+def test_matches_oracle_and_gemm_sgemm_f32_on_two_calls_in_a_row(w):
     inputs = workloads.make_inputs(w)
     dev = parity.to_device(inputs)
-    ref_c = _call(gemm_sgemm_f32, w, dev, dev["C"])
-    _, absdot = parity.oracle_full(w, inputs)
+    ref, absdot = parity.oracle_full(w, inputs)
     cin = inputs["C"].numpy()[:, : w.N] if w.beta != 0.0 else None
+    lib = _call(gemm_sgemm_f32, w, dev, dev["C"]).cpu().numpy()[:, : w.N]
     first = _call(gemm_sgemm_f32_noalloc, w, dev, dev["C"])
     second = _call(gemm_sgemm_f32_noalloc, w, dev, dev["C"])
-    ref = ref_c.cpu().numpy()[:, : w.N]
     for got in (first, second):
-        parity.assert_close(w, got.cpu().numpy()[:, : w.N], ref, absdot, cin)
+        g = got.cpu().numpy()[:, : w.N]
+        parity.assert_close(w, g, ref, absdot, cin, where=" (against the oracle)")
+        parity.assert_close(w, g, lib, absdot, cin, where=" (against gemm_sgemm_f32)")
     # the split-K sum has a fixed order: the two calls agree bit for bit
     f, s2 = first[:, : w.N].contiguous(), second[:, : w.N].contiguous()
     assert torch.equal(f.view(torch.int32), s2.view(torch.int32))
@@ -53,11 +58,11 @@ def test_matches_gemm_sgemm_f32_on_two_calls_in_a_row(w):
         assert torch.isnan(first[:, w.N:]).all() and torch.isnan(second[:, w.N:]).all()
 
 
-def test_oversized_problem_is_refused_without_launch():
-    # 4096 x 4096 has 4096 tiles of 64 x 64: their partials would not fit the scratch array
-    A = torch.zeros(16, 16, device="cuda")
+def test_sizes_beyond_the_limit_are_refused_without_launch():
+    # M = 2^31 is beyond the entry point's limit: refused on the host, nothing launched
+    A = torch.zeros(16, device="cuda")
     with pytest.raises(GemmError) as e:
-        gemm_sgemm_f32_noalloc("N", "N", 4096, 4096, 16, 1.0, A, 16, A, 4096, 0.0, A, 4096)
+        gemm_sgemm_f32_noalloc("N", "N", 1 << 31, 1, 1, 1.0, A, 1, A, 1, 0.0, A, 1)
     assert e.value.status == 3  # GEMM_ERR_UNSUPPORTED
 
 
@@ -66,8 +71,8 @@ def test_integer_inputs_bit_exact_against_oracle():
                            dist_b="int4")
     inputs = workloads.make_inputs(w)
     dev = parity.to_device(inputs)
+    ref = oracle.gemm("N", "N", w.M, w.N, w.K, 1.0, inputs["A"].numpy(), w.lda,
+                      inputs["B"].numpy(), w.ldb)
     for _ in range(2):
         C = _call(gemm_sgemm_f32_noalloc, w, dev, dev["C"])
-        ref = oracle.gemm("N", "N", w.M, w.N, w.K, 1.0, inputs["A"].numpy(), w.lda,
-                          inputs["B"].numpy(), w.ldb)
         assert np.array_equal(C.cpu().numpy().view(np.uint32), ref.view(np.uint32))
