@@ -1,19 +1,25 @@
 """Benchmark of the GEMM library on one GB300 (or N independent replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-suite]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-suite] [--no-cpu-baseline] [--no-cublas]
 
-A step is one call of the library on the headline workload: the strict-FP32 ragged
-problem M=1001, N=777, K=513, alpha=1.5, beta=-0.5 (uniform[-1,1] inputs from seed 1), the
-1001 x 513 x 777 case of the yekq.top "LeetGPU 第二题" page that exercises every tail of
-the tile grid.  Inputs are resident in HBM when the timed region starts; the 9.9 MB
-working set fits in L2, so L2 is flushed (a 512 MB write) before every timed step and
-only the GEMM itself sits between each step's CUDA events.
+A step is one call of the library on the headline workload, by default the largest of the
+configurations: fp16 inputs, fp32 accumulation and output, M = N = K = 8192, alpha = 1,
+beta = 0 (uniform[-1,1] inputs rounded to fp16, seed 3; 1.1 TFLOP per call).  Inputs are
+resident in HBM when the timed region starts; L2 is flushed (a 512 MB write) before every
+timed step, so only the GEMM itself sits between each step's CUDA events.
 
 Printed: ONE JSON line (rank 0) with the throughput (2*M*N*K / device time, TFLOP/s), the
 roofline of the kernel, the CPU oracle timed on the host cores, the end-to-end number
 through the public API with host buffers, the SM clocks seen during the timed region and,
-under "suite", the other headline shapes (fp32 4096^3 and 16384^2 x 1024, fp16 4096^3,
-8192^3 and the linear-layer 16384 x 4096 x 4096 problem) timed the same way.
+under "suite", every configuration of the method (SGEMM 256^3 and its integer twin, the
+ragged 1001 x 777 x 513 problem, the M = N sweep 128 ... 16384 with K = 1024, 4096^3; HGEMM
+2048^3, 4096^3, 8192^3 and the integer 2048 x 2048 x 1024 twin; the linear-layer problem
+16384 x 4096 x 4096 with op(B) = T and beta = 1), each timed the same way: min, median and
+max device time, TFLOP/s, fraction of the roofline, achieved HBM bandwidth (compulsory
+bytes / median time), launches per call, the clocks sampled while it ran, cuBLAS through
+torch as a side column and, for the two small SGEMM configurations, the oracle's time on
+one core and on all cores.
 
 --impl reference times the CPU oracle (the only reference implementation of this path)
 on the same workload, on rank 0 only, as bounded row-slab samples.
@@ -73,11 +79,12 @@ class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.samples = []  # (monotonic time of arrival, csv line)
         self.thread = None
 
     def start(self):
@@ -95,20 +102,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, maximum clock, throttle reasons seen and peak power of the samples
+        that arrived in [t0, t1] (all samples when no window is given)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=5)
         sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in list(self.samples):
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -118,13 +122,24 @@ class ClockSampler:
                 power.append(float(parts[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(self.REASONS, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_max": max(power) if power else None}
+
+    def stop(self):
+        if self.proc is None:
+            return self.summary()
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        return self.summary()
 
 
 # ------------------------------------------------------------------ helpers
@@ -343,6 +358,18 @@ def run_reference(args, rank, world):
     return 0
 
 
+def _roofline_peak(w, peaks):
+    """Compute peak of the path (TFLOP/s), its kind and source, and the roofline of this
+    problem: the lesser of the compute peak and intensity x measured HBM bandwidth."""
+    if w.dtype == "f32":
+        peak, bound, src = FFMA_PEAK_TFLOPS, "alu", "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
+    else:
+        peak, bound = peaks["bf16_tflops"], "tensor"
+        src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
+    hbm_roof = w.flops / w.algorithmic_bytes * peaks["hbm_gbs"] / 1e3
+    return peak, bound, src, min(peak, hbm_roof)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -364,8 +391,9 @@ def run_ours(args, rank, world, local):
     host, dev = _device_inputs(w)
     clocks = ClockSampler(local)
     clocks.start()
+    t0 = time.monotonic()
     step_ms, wall, launches = time_device(w, dev, args.steps, args.warmup, flush, barrier)
-    clk = clocks.stop()
+    clk = clocks.summary(t0, time.monotonic())
     status = lib.gemm_get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {lib.gemm_status_string(status)}")
@@ -373,13 +401,8 @@ def run_ours(args, rank, world, local):
                                       torch.device("cuda", local))
     mean_ms = statistics.fmean(step_ms)
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
-    if w.dtype == "f32":
-        kernel = "sgemm_ffma"
-        bound, peak, peak_src = "alu", FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
-    else:
-        kernel = "hgemm_tcgen05"
-        bound, peak = "tensor", peaks["bf16_tflops"]
-        peak_src = f"bf16 dense burst ({peaks['source']}); fp16 has the same nominal rate"
+    kernel = "sgemm_ffma" if w.dtype == "f32" else "hgemm_tcgen05"
+    peak, bound, peak_src, roof = _roofline_peak(w, peaks)
     traffic = _traffic_from_profile(kernel, f"{kernel}_{w.name}.txt")
     # The library's own FFMA-chain probe, run after the timed region: a measured FP32
     # multiply-add ceiling beside the one derived from unit counts and the maximum clock.
@@ -401,6 +424,9 @@ def run_ours(args, rank, world, local):
                      "peak": round(peak, 2), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": w.algorithmic_bytes, "peak_source": peak_src,
+                     "roof": round(roof, 2), "frac_of_roof": round(achieved / roof, 4),
+                     "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                           if w.dtype != "f32" else None),
                      "peak_fma_probe": probe,
                      "median_ms": round(statistics.median(step_ms), 5),
                      "min_ms": round(min(step_ms), 5), "max_ms": round(max(step_ms), 5)},
@@ -410,9 +436,14 @@ def run_ours(args, rank, world, local):
     }
     e2e_steps = max(3, min(args.steps, 200))
     line["e2e"] = time_e2e(w, host, e2e_steps)
+    del host, dev
+    torch.cuda.empty_cache()
     if rank == 0 and not args.no_suite:
-        line["suite"] = run_suite(peaks, flush)
+        line["suite"] = run_suite(peaks, flush, clocks, cublas=not args.no_cublas,
+                                  oracle_times=not args.no_cpu_baseline)
+    clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = workloads.make_inputs(w)
         rows, threads, run = oracle_sample(w, host, 1.0)
         reps = max(1, int(10.0 / max(run(rows), 1e-3)))
         times = [run(rows) for _ in range(reps)]
@@ -431,27 +462,102 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def run_suite(peaks, flush):
-    """The other headline shapes, timed like the main step (median of 20, L2 flushed)."""
-    import torch
-
+# Every configuration of the method; the pages' own figure where one exists for that exact
+# problem (their hardware, context only).
+def suite_workloads():
     from dense_gemm_sgemm_gb300 import workloads
 
+    out = [workloads.sgemm_256(), workloads.sgemm_256(integer=True), workloads.sgemm_ragged()]
+    out += [workloads.sgemm_sweep(mn) for mn in workloads.SWEEP_MN]
+    out += [workloads.sgemm_cube(4096)]
+    out += [workloads.hgemm_square(n) for n in workloads.HGEMM_SQUARE]
+    out += [workloads.hgemm_square(2048, integer=True, K=1024), workloads.linear_fp16()]
+    return out
+
+
+PAGES_CONTEXT = {
+    "sgemm_ragged_1001x777x513": "13.85 TFLOP/s, v4 2-D register coarsening, RTX 4090 (yekq.top)",
+    "sgemm_sweep_16384x16384x1024": "12.66 TFLOP/s, V3 double buffer, V100 (ssxxe.cn)",
+    "hgemm_4096x4096x4096": "103.10 TFLOP/s, WMMA v7, RTX 5080 (dandandamowang.xyz)",
+}
+
+
+def _cublas_call(w, dev):
+    """torch.matmul on the same operands (cuBLAS; TF32 off for fp32).  Its fp16 GEMM writes
+    fp16 and ignores alpha, beta and C_in: a side reference, not the same output."""
+    import torch
+
+    A = dev["A"][:, : w.a_shape[1]]
+    B = dev["B"][:, : w.b_shape[1]]
+    a = A if w.opA == "N" else A.t()
+    b = B if w.opB == "N" else B.t()
+    return lambda: torch.matmul(a, b)
+
+
+def _time_fn(fn, reps, warmup, flush):
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def run_suite(peaks, flush, clocks, cublas=True, oracle_times=True):
+    """Every configuration, timed like the headline step (L2 flushed before each timed call):
+    at least 30 calls and about 0.2 s of calls per configuration."""
+    import torch
+
+    torch.backends.cuda.matmul.allow_tf32 = False
     out = []
-    fp16_peak = peaks["bf16_tflops"]  # fp16 and bf16 have the same nominal tensor rate
-    for w in (workloads.sgemm_cube(4096), workloads.sgemm_sweep(16384),
-              workloads.hgemm_square(4096), workloads.hgemm_square(8192), workloads.linear_fp16()):
+    for w in suite_workloads():
         host, dev = _device_inputs(w)
-        ms, _, launches = time_device(w, dev, 20, 5, flush)
+        probe_ms, _, _ = time_device(w, dev, 3, 3, flush)
+        reps = int(min(400, max(30, 0.2 / (statistics.median(probe_ms) * 1e-3 + 1e-4))))
+        t0 = time.monotonic()
+        ms, _, launches = time_device(w, dev, reps, 5, flush)
+        clk = clocks.summary(t0, time.monotonic())
         med = statistics.median(ms)
         tf = w.flops / (med * 1e-3) / 1e12
-        peak = FFMA_PEAK_TFLOPS if w.dtype == "f32" else fp16_peak
-        out.append({"workload": w.name, "dtype": w.dtype, "tflops": round(tf, 2),
-                    "median_ms": round(med, 4), "peak": round(peak, 1),
-                    "bound": "alu" if w.dtype == "f32" else "tensor",
-                    "frac": round(tf / peak, 4), "launches_per_call": launches / 20,
-                    "peak_source": ("152 SMs x 128 x 2 x 2.07 GHz" if w.dtype == "f32"
-                                    else f"bf16 burst ({peaks['source']}), fp16 same nominal rate")})
+        peak, bound, src, roof = _roofline_peak(w, peaks)
+        entry = {"workload": w.name, "dtype": w.dtype, "M": w.M, "N": w.N, "K": w.K,
+                 "opA": w.opA, "opB": w.opB, "alpha": w.alpha, "beta": w.beta, "reps": reps,
+                 "min_us": round(min(ms) * 1e3, 2), "median_us": round(med * 1e3, 2),
+                 "max_us": round(max(ms) * 1e3, 2), "tflops": round(tf, 3),
+                 "bound": bound, "peak": round(peak, 1), "frac": round(tf / peak, 4),
+                 "roof": round(roof, 1), "frac_of_roof": round(tf / roof, 4),
+                 "hbm_gbs": round(w.algorithmic_bytes / (med * 1e-3) / 1e9, 1),
+                 "hbm_frac": round(w.algorithmic_bytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                 "algorithmic_bytes": w.algorithmic_bytes,
+                 "launches_per_call": launches / reps, "clocks": clk, "peak_source": src}
+        if w.name in PAGES_CONTEXT:
+            entry["pages"] = PAGES_CONTEXT[w.name]
+        if cublas:
+            cms = _time_fn(_cublas_call(w, dev), min(reps, 100), 5, flush)
+            entry["cublas_tflops"] = round(w.flops / (statistics.median(cms) * 1e-3) / 1e12, 3)
+            entry["cublas_note"] = ("torch.matmul, TF32 off" if w.dtype == "f32"
+                                    else "torch.matmul, fp16 output, no alpha/beta")
+        if oracle_times and w.name.startswith(("sgemm_256cube", "sgemm_ragged")):
+            import oracle
+
+            for key, threads in (("oracle_1core_s", 1), ("oracle_all_cores_s", oracle.default_threads())):
+                t = time.perf_counter()
+                oracle.gemm(w.opA, w.opB, w.M, w.N, w.K, w.alpha, host["A"].numpy(), w.lda,
+                            host["B"].numpy(), w.ldb, w.beta,
+                            host["C"].numpy() if w.beta != 0.0 else None, w.ldc, threads=threads)
+                entry[key] = round(time.perf_counter() - t, 4)
+            entry["oracle_cores"] = oracle.default_threads()
+        out.append(entry)
         del host, dev
         torch.cuda.empty_cache()
     return out
@@ -460,12 +566,13 @@ def run_suite(peaks, flush):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="sgemm_ragged_1001x777x513",
+    ap.add_argument("--workload", default="hgemm_8192x8192x8192",
                     help="workload of the timed step (names in dense_gemm_sgemm_gb300.workloads)")
-    ap.add_argument("--no-suite", action="store_true", help="skip the other headline shapes")
+    ap.add_argument("--no-suite", action="store_true", help="skip the per-configuration suite")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS side column")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
     args = ap.parse_args(argv)
     if args.warmup < 3:

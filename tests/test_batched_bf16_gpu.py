@@ -33,7 +33,7 @@ def test_bf16_small_full_oracle(opA, opB):
     parity.check_full(w, inputs, dev["C"][:, : w.N].contiguous())
 
 
-def test_bf16_integer_bit_exact_and_large_sampled():
+def test_bf16_integer_bit_exact_and_large_full_oracle():
     w = workloads.Workload("bf16_int", "bf16", 2304, 2560, 512, opB="T", seed=42,
                            dist_a="int4", dist_b="int4")
     inputs = workloads.make_inputs(w)
@@ -47,7 +47,7 @@ def test_bf16_integer_bit_exact_and_large_sampled():
     parity.run_library(w, dev)
     torch.cuda.synchronize()
     assert gemm_get_device_status() == 0
-    parity.check_sampled(w, inputs, dev["C"], n_random=1024)
+    parity.check_full(w, inputs, dev["C"])
 
 
 # --------------------------------------------------------------------- strided batched
