@@ -65,7 +65,7 @@ constexpr int kTmemCols = 2 * BN;   // two accumulators
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int EPI_BYTES = 4 * 32 * 32 * 4;  // a 32 x 32 fp32 staging tile per epilogue warp
 constexpr int kBarBytes = 256;
-constexpr int kLogGroup = 3;
+constexpr int kLogGroup = 3;  // default raster group: 2^3 tile rows (or tile-pair rows)
 
 // Ring geometry of the two forms: a CTA of a pair holds half of the B columns.
 template <bool PAIR>
@@ -112,6 +112,7 @@ struct HgemmParams {
     int a_batched, b_batched;  // 0: the operand is shared by every problem (stride 0)
     int64_t stride_c;          // elements between consecutive C matrices
     uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
+    int log_group;             // raster group of 2^log_group tile (pair) rows
 };
 
 constexpr int kTailNone = 0, kTailN = 1, kTailK = 2;
@@ -489,7 +490,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 const int n_off = x.n_off, width = x.width;
                 int64_t tm, tn;
                 const int64_t bt = t / p.per_batch;
-                raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
+                raster(t - bt * p.per_batch, rows_r, p.tiles_n, p.log_group, tm, tn);
                 if (PAIR) tm = 2 * tm + rank;
                 const int32_t ba = p.a_batched ? static_cast<int32_t>(bt) : 0;
                 const int32_t bb = p.b_batched ? static_cast<int32_t>(bt) : 0;
@@ -634,7 +635,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             const int n_off = x.n_off, width = x.width;
             int64_t tm, tn;
             const int64_t bt = t / p.per_batch;
-            raster(t - bt * p.per_batch, rows_r, p.tiles_n, kLogGroup, tm, tn);
+            raster(t - bt * p.per_batch, rows_r, p.tiles_n, p.log_group, tm, tn);
             if (PAIR) tm = 2 * tm + rank;
             // The four epilogue warps leave together or not at all: a K-half unit below
             // synchronises them, so none may have given up on a unit the others continue.
@@ -996,6 +997,10 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     p.ab_format = bf ? 1u : 0u;
     p.timeout_ns = 2000000000ull;
     p.inject_stall = 0;
+    // GEMM_GB300_HGEMM_GROUP=g (sweeps only): a raster group of 2^g tile (pair) rows
+    p.log_group = kLogGroup;
+    if (const char *e = std::getenv("GEMM_GB300_HGEMM_GROUP"); e && e[0] >= '0' && e[0] <= '9' && !e[1])
+        p.log_group = e[0] - '0';
     if (const char *e = std::getenv("GEMM_GB300_TEST_INJECT_STALL"); e && (e[0] == '1' || e[0] == '2')) {
         p.inject_stall = e[0] - '0';
         p.timeout_ns = 20000000ull;
