@@ -1,7 +1,7 @@
 """Benchmark of the GEMM library on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-suite] [--no-cpu-baseline] [--no-cublas]
+                    [--workload NAME] [--no-suite] [--no-cpu-baseline] [--no-cublas] [--no-e2e]
 
 A step is one call of the library on the headline workload, by default the largest of the
 configurations: fp16 inputs, fp32 accumulation and output, M = N = K = 8192, alpha = 1,
@@ -434,8 +434,8 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
     }
-    e2e_steps = max(3, min(args.steps, 200))
-    line["e2e"] = time_e2e(w, host, e2e_steps)
+    if not args.no_e2e:
+        line["e2e"] = time_e2e(w, host, max(3, min(args.steps, 200)))
     del host, dev
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_suite:
@@ -574,6 +574,8 @@ def main(argv=None):
     ap.add_argument("--no-suite", action="store_true", help="skip the per-configuration suite")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS side column")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg through the host-memory entry point")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
