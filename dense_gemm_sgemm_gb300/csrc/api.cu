@@ -134,23 +134,9 @@ static gemm_status_t tc_impl(int dtype, int opA, int opB, int64_t M, int64_t N, 
         if (beta == 1.0f) return GEMM_OK;
         return from_cuda(launch_scale_batched(M, N, beta, C, ldc, strideC, batch, st));
     }
-    // Operands the tensor-memory-access unit cannot read directly (base not 16-byte aligned,
-    // leading dimension or batch stride not a multiple of 8 elements) are packed first.
-    auto tma_ok = [&](const void *p, int64_t ld, int64_t stride) {
-        return aligned(p, 16) && ld % 8 == 0 && (batch <= 1 || stride % 8 == 0);
-    };
-    if (!tma_ok(A, lda, strideA)) {
-        const int64_t rows = opA == GEMM_OP_N ? M : K, cols = opA == GEMM_OP_N ? K : M;
-        if (!pack_u16_operand(dev.device, st, 0, A, rows, cols, lda, batch > 1 ? strideA : 0, batch, &A, &lda,
-                              &strideA))
-            return GEMM_ERR_MISALIGNED;
-    }
-    if (!tma_ok(B, ldb, strideB)) {
-        const int64_t rows = opB == GEMM_OP_N ? K : N, cols = opB == GEMM_OP_N ? N : K;
-        if (!pack_u16_operand(dev.device, st, 1, B, rows, cols, ldb, batch > 1 ? strideB : 0, batch, &B, &ldb,
-                              &strideB))
-            return GEMM_ERR_MISALIGNED;
-    }
+    // Operands the tensor-memory-access unit cannot read (base not 16-byte aligned, leading
+    // dimension or batch stride not a multiple of 8 elements) are read by the kernel's loader
+    // warps instead, in the same launch.
     return launch_hgemm(dev, dtype, opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
                         strideC, batch, st);
 }

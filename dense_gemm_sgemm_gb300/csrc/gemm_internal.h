@@ -68,20 +68,13 @@ cudaError_t launch_scale(int64_t M, int64_t N, float beta, float *C, int64_t ldc
 constexpr int kInF16 = 0;
 constexpr int kInBf16 = 1;
 
-// Returns GEMM_OK, GEMM_ERR_MISALIGNED or GEMM_ERR_LAUNCH.
+// Returns GEMM_OK, GEMM_ERR_MISALIGNED or GEMM_ERR_LAUNCH.  A and B need only 2-byte
+// alignment: operands that TMA cannot read go through the kernel's loader warps.
 gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, int64_t M,
                            int64_t N, int64_t K, float alpha, const uint16_t *A, int64_t lda,
                            int64_t strideA, const uint16_t *B, int64_t ldb, int64_t strideB,
                            float beta, float *C, int64_t ldc, int64_t strideC, int64_t batch,
                            cudaStream_t stream);
-
-// Copies a 16-bit operand (batch x rows x cols, leading dimension ld, batch stride stride;
-// stride 0 = shared) into this stream's scratch buffer `which` (0 = A, 1 = B) with the
-// leading dimension rounded up to 8, so the tensor-memory-access unit can read it.  Returns
-// the packed pointer, leading dimension and stride; false when no buffer can be had.
-bool pack_u16_operand(int dev, cudaStream_t stream, int which, const uint16_t *src, int64_t rows,
-                      int64_t cols, int64_t ld, int64_t stride, int64_t batch, const uint16_t **out,
-                      int64_t *ld_out, int64_t *stride_out);
 
 // Writes the transpose of an fp32 operand (batch x rows x cols, leading dimension ld, batch
 // stride stride; stride 0 = shared) into this stream's scratch buffer `which` (0 = A, 1 = B)

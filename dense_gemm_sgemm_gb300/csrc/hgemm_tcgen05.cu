@@ -47,6 +47,7 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "gemm_internal.h"
@@ -60,6 +61,9 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;  // BM: rows per CTA
 constexpr int kThreads = 192;  // 6 warps
+constexpr int kLdgThreads = 192;  // issuer warps 6-7 and fixer warps 8-11 of the loader form
+template <bool LDG>
+constexpr int threads_of() { return LDG ? kThreads + kLdgThreads : kThreads; }
 constexpr int kAccCols = BN;        // fp32 columns per accumulator
 constexpr int kTmemCols = 2 * BN;   // two accumulators
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
@@ -67,18 +71,27 @@ constexpr int EPI_BYTES = 4 * 32 * 32 * 4;  // a 32 x 32 fp32 staging tile per e
 constexpr int kBarBytes = 256;
 constexpr int kLogGroup = 3;  // default raster group: 2^3 tile rows (or tile-pair rows)
 
-// Ring geometry of the two forms: a CTA of a pair holds half of the B columns.
-template <bool PAIR>
+// Ring geometry of the forms: a CTA of a pair holds half of the B columns.  The loader form
+// keeps, per stage, a 16-byte side slot for every stage row (the ninth block of a row that is
+// not 16-byte aligned), and fewer stages: its copies pass through the L1 data array, whose
+// size -- what the shared-memory carve-out leaves of the 256 KB -- bounds the bytes they can
+// have in flight (4 stages of a pair: 164 KB carve-out, 92 KB of L1).
+template <bool PAIR, bool LDG = false>
 struct Ring {
-    static constexpr int kStages = PAIR ? 6 : 4;
-    static constexpr int kBStageBytes = (PAIR ? BN / 2 : BN) * BK * 2;  // 16 KB or 32 KB
+    static constexpr int kStages = LDG ? (PAIR ? 4 : 3) : (PAIR ? 6 : 4);
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;
+    static constexpr int kBStageBytes = kBRows * BK * 2;  // 16 KB or 32 KB
     static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
-    static constexpr int kSmemBytes = kStages * kStageBytes + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
+    static constexpr int kSideBytes = LDG ? (BM + kBRows) * 16 : 0;  // per stage
+    static constexpr int kSmemBytes =
+        kStages * (kStageBytes + kSideBytes) + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
 };
-static_assert(Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024,
+static_assert(Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024 &&
+                  Ring<true, true>::kSmemBytes <= 227 * 1024 && Ring<false, true>::kSmemBytes <= 227 * 1024,
               "one CTA per SM within the 227 KB opt-in limit");
-constexpr int kMaxSmemBytes =
-    Ring<true>::kSmemBytes > Ring<false>::kSmemBytes ? Ring<true>::kSmemBytes : Ring<false>::kSmemBytes;
+template <bool LDG>
+constexpr int max_smem_of() { return Ring<true, LDG>::kSmemBytes > Ring<false, LDG>::kSmemBytes ? Ring<true, LDG>::kSmemBytes : Ring<false, LDG>::kSmemBytes; }
+constexpr int kMaxSmemBytes = max_smem_of<false>() > max_smem_of<true>() ? max_smem_of<false>() : max_smem_of<true>();
 
 struct HgemmParams {
     int64_t M, N, K;
@@ -113,6 +126,12 @@ struct HgemmParams {
     int64_t stride_c;          // elements between consecutive C matrices
     uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
     int log_group;             // raster group of 2^log_group tile (pair) rows
+    // Operands the tensor-memory-access unit cannot read (base not 16-byte aligned, leading
+    // dimension or batch stride not a multiple of 8 elements) are read by the loader warps:
+    // pointer, leading dimension and batch stride of the stored matrix, in elements.
+    int a_ldg, b_ldg;
+    const uint16_t *a_ptr, *b_ptr;
+    int64_t lda, ldb, stride_a, stride_b;
 };
 
 constexpr int kTailNone = 0, kTailN = 1, kTailK = 2;
@@ -174,28 +193,41 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for phases completed by release arrivals of threads of
+// the other CTA of a pair.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up (returns false) when the
 // CTA-wide abort flag is raised or after timeout_ns nanoseconds.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag,
                                           uint64_t timeout_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if ((it & 15u) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) return false;
@@ -405,17 +437,220 @@ __host__ __device__ constexpr uint32_t make_idesc(int a_mn, int b_mn, int n, int
            (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ loader warps
+// For an operand whose rows TMA cannot address (its copies need a 16-byte aligned base and
+// 16-byte multiples as row and batch strides), the loader form of the kernel fills the same
+// swizzled stages as TMA would, in two roles:
+//   issuer warps 6-7  copy each stage row as the aligned 16-byte blocks that cover it with
+//                     cp.async (the cp.async producer of dandandamowang "GEMM优化（二）",
+//                     section 5 (v4)); completion is counted on the stage's "copied" barrier
+//                     (cp.async.mbarrier.arrive), so they never wait for their own copies and
+//                     run ahead as far as the ring has free slots;
+//   fixer warps 8-11  wait for a stage's copies, shift the rows that do not start on a 16-byte
+//                     boundary into place, order the stage before the tensor cores' reads
+//                     (proxy fence) and announce it on the (rank 0) full barrier.
+// Both roles decide row by row with the same functions below, so they agree on which rows
+// were copied as blocks and which need shifting.
+constexpr int kIssuers = 64, kFixers = 128;
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t dst, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t src)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(src)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u16(const uint16_t *p)
+{
+    return __ldcg(reinterpret_cast<const unsigned short *>(p));
+}
+
+// OR of `pred` over the COUNT threads of named barrier ID; every one of them must call it.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool group_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(ID), "n"(COUNT)
+        : "memory");
+    return r != 0;
+}
+
+// Stage row r of an operand for the K slice at k0 holds 64 elements of one row of the stored
+// matrix `mat` (leading dimension ld): for a K-major operand (MN = false) row `first + r` from
+// column k0, for an MN-major one row k0 + r % 64 from column first + 64 (r / 64) -- the boxes
+// TMA would copy.  Chunk c of row r belongs at dst + 128 r + 16 (c ^ (r % 8)), the 128-byte
+// swizzle of the tensor maps.  Elements outside the stored matrix (mn x K for K-major, K x mn
+// for MN-major) are zeros.  A row entirely inside the matrix is copied as the aligned 16-byte
+// blocks that cover it: block b into the place of chunk b and, when the row starts delta > 0
+// bytes into a block ("shifted"), block 8 into side + 16 r.  These blocks reach up to 14 bytes
+// before and 16 after the row's 128, always inside the operand's own storage
+// [mat, mat + (rows - 1) ld + cols) -- a row whose blocks would not be (at the very start or
+// end of that storage), and a row cut by the matrix edge, is read element by element.
+struct RowPlan {
+    uintptr_t a0;      // first block
+    int64_t grow, gcol;  // stored row and column of the row's element 0
+    int64_t left;      // elements of the row inside the matrix from gcol (0: outside)
+    bool blocks, shifted;
+};
+
+template <bool MN>
+__device__ __forceinline__ RowPlan row_plan(const uint16_t *mat, int64_t ld, int64_t mn, int64_t K, int64_t first,
+                                            int64_t k0, int r)
+{
+    const int64_t rows_total = MN ? K : mn, cols_total = MN ? mn : K;
+    RowPlan x;
+    x.grow = MN ? k0 + (r & 63) : first + r;
+    x.gcol = MN ? first + 64 * (r >> 6) : k0;
+    x.left = x.grow < rows_total ? cols_total - x.gcol : 0;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(mat + x.grow * ld + x.gcol);
+    x.a0 = s & ~uintptr_t(15);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(mat);
+    const uintptr_t hi = lo + 2u * uintptr_t((rows_total - 1) * ld + cols_total);
+    x.blocks = x.left >= 64 && (x.a0 == s || (x.a0 >= lo && x.a0 + 144u <= hi));
+    x.shifted = x.blocks && x.a0 != s;
+    return x;
+}
+
+// True when every row of the R-row box is inside the matrix and its blocks inside the
+// storage: the rows need no individual checks.
+template <bool MN>
+__device__ __forceinline__ bool box_interior(int64_t mn, int64_t K, int64_t first, int64_t k0, int R)
+{
+    return MN ? (k0 + 64 <= K && first + 64 * (R / 64) <= mn && (k0 > 0 || first >= 8) &&
+                 (k0 + 64 < K || first + 64 * (R / 64) + 8 <= mn))
+              : (first + R <= mn && k0 + 64 <= K && (first > 0 || k0 >= 8) && (first + R < mn || k0 + 72 <= K));
+}
+
+// Issuer thread ti (0..63) copies chunk c = ti % 8 of rows ti / 8 + 8 i, i < R / 8.  Rows
+// congruent modulo 8 lie a multiple of 16 bytes apart (16 ld bytes, or 128 across MN-major
+// boxes), so all of this thread's rows share one offset within a 16-byte block.  Rows read
+// element by element are stored before this returns (in groups of 8 chunks, so the loads of
+// a group are in flight together).
+template <bool MN, int R>
+__device__ __forceinline__ void ldg_issue(uint32_t dst, uint32_t side, const uint16_t *mat, int64_t ld,
+                                          int64_t mn, int64_t K, int64_t first, int64_t k0, int ti)
+{
+    constexpr int N = R / 8;  // rows of this thread
+    const int c = ti & 7, rho = ti >> 3;
+    if (box_interior<MN>(mn, K, first, k0, R)) {
+        const uintptr_t s = reinterpret_cast<uintptr_t>(MN ? mat + (k0 + rho) * ld + first : mat + (first + rho) * ld + k0);
+        const uintptr_t a0 = s & ~uintptr_t(15);
+        const uintptr_t ld16 = 16u * uintptr_t(ld);  // bytes between rows 8 apart
+        const bool shifted = a0 != s;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int r = rho + 8 * i;
+            const uintptr_t a = a0 + (MN ? uintptr_t(i & 7) * ld16 + uintptr_t(i >> 3) * 128u : uintptr_t(i) * ld16);
+            cp_async_16(dst + uint32_t(r) * 128u + (uint32_t(c ^ rho) << 4), reinterpret_cast<const void *>(a + 16u * c));
+            if (shifted && c == 7) cp_async_16(side + 16u * uint32_t(r), reinterpret_cast<const void *>(a + 128u));
+        }
+        return;
+    }
+#pragma unroll
+    for (int i0 = 0; i0 < N; i0 += 8) {
+        uint4 v[8];
+        uint32_t store = 0;
+#pragma unroll
+        for (int j = 0; j < 8 && i0 + j < N; ++j) {
+            const int r = rho + 8 * (i0 + j);
+            const RowPlan x = row_plan<MN>(mat, ld, mn, K, first, k0, r);
+            const uint32_t sdst = dst + uint32_t(r) * 128u + (uint32_t(c ^ rho) << 4);
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (x.blocks) {
+                cp_async_16(sdst, reinterpret_cast<const void *>(x.a0 + 16u * c));
+                if (x.shifted && c == 7) cp_async_16(side + 16u * uint32_t(r), reinterpret_cast<const void *>(x.a0 + 128u));
+                continue;
+            }
+            const int64_t left = x.left - 8 * c;
+            const int nv = left <= 0 ? 0 : left >= 8 ? 8 : int(left);
+            if (nv > 0) {
+                const uint16_t *src = mat + x.grow * ld + x.gcol + 8 * c;
+                uint32_t e[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) e[k] = k < nv ? ldg_u16(src + k) : 0u;
+                v[j] = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+            }
+            store |= 1u << j;
+        }
+#pragma unroll
+        for (int j = 0; j < 8 && i0 + j < N; ++j)
+            if ((store >> j) & 1u) {
+                const int r = rho + 8 * (i0 + j);
+                st_shared_v4(dst + uint32_t(r) * 128u + (uint32_t(c ^ rho) << 4), v[j]);
+            }
+    }
+}
+
+// Fixer thread tf (0..127, fixer warp w = tf / 32, lanes 8g..8g+7 one row) shifts, in
+// iteration i < R / 16, row w + 4 (i % 2) + 8 (g + 4 (i / 2)) if it was copied shifted: chunk
+// c = tf % 8 becomes bytes [delta, delta + 16) of block c followed by block c + 1 (block 8 from
+// the side slot).  The rows of one warp instruction are congruent modulo 8 and share delta,
+// so the word selection does not diverge; the eight lanes of a row read before any writes.
+// Every fixer thread must call this.
+template <bool MN, int R>
+__device__ __forceinline__ void ldg_fix(uint32_t dst, uint32_t side, const uint16_t *mat, int64_t ld,
+                                        int64_t mn, int64_t K, int64_t first, int64_t k0, int tf)
+{
+    const int w = tf >> 5, g = (tf >> 3) & 3, c = tf & 7;
+    const bool interior = box_interior<MN>(mn, K, first, k0, R);
+    // offset of residue rho's rows within their 16-byte blocks (the same in every row
+    // congruent to rho modulo 8, see ldg_issue)
+    const uint32_t mat_b = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(mat));
+    const uint32_t seed = (MN ? mat_b + 2u * uint32_t(first) + 2u * uint32_t(ld) * uint32_t(k0)
+                              : mat_b + 2u * uint32_t(ld) * uint32_t(first) + 2u * uint32_t(k0)) & 15u;
+#pragma unroll
+    for (int i = 0; i < R / 16; ++i) {
+        const int rho = w + 4 * (i & 1), r = rho + 8 * (g + 4 * (i >> 1));
+        const uint32_t delta = (seed + 2u * uint32_t(ld) * uint32_t(rho)) & 15u;
+        const bool fix = interior ? delta != 0 : row_plan<MN>(mat, ld, mn, K, first, k0, r).shifted;
+        const uint32_t pos = dst + uint32_t(r) * 128u + (uint32_t(c ^ rho) << 4);
+        const uint32_t pos1 = c < 7 ? dst + uint32_t(r) * 128u + (uint32_t((c + 1) ^ rho) << 4)
+                                    : side + 16u * uint32_t(r);
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (fix) {
+            const uint4 x = ld_shared_v4(pos), y = ld_shared_v4(pos1);
+            const uint32_t sh = (delta & 3u) * 8u;
+            auto f = [sh](uint32_t lo, uint32_t hi) { return __funnelshift_r(lo, hi, sh); };
+            switch (delta >> 2) {
+            case 0: o = make_uint4(f(x.x, x.y), f(x.y, x.z), f(x.z, x.w), f(x.w, y.x)); break;
+            case 1: o = make_uint4(f(x.y, x.z), f(x.z, x.w), f(x.w, y.x), f(y.x, y.y)); break;
+            case 2: o = make_uint4(f(x.z, x.w), f(x.w, y.x), f(y.x, y.y), f(y.y, y.z)); break;
+            default: o = make_uint4(f(x.w, y.x), f(y.x, y.y), f(y.y, y.z), f(y.z, y.w)); break;
+            }
+        }
+        __syncwarp();
+        if (fix) st_shared_v4(pos, o);
+    }
+}
+
 // ------------------------------------------------------------------ the kernel
 // PAIR = false: one CTA per 128 x 256 tile.  PAIR = true: units count tile pairs along M;
 // the CTA of cluster rank r computes tile row 2 * pair_row + r, and rank 0 issues the
-// pair's MMAs.
-template <int A_MN, int B_MN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+// pair's MMAs.  LDG = true: four more warps (6-9) load the operands flagged a_ldg / b_ldg
+// into the ring themselves and warp 10 relays their slices to the MMA issuer; the producer
+// warp still arms each slice and copies the other operand (if any) by TMA.
+template <int A_MN, int B_MN, bool PAIR, bool LDG>
+__global__ void __launch_bounds__(threads_of<LDG>(), 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_b_half,
                      const __grid_constant__ CUtensorMap map_b_quarter, const HgemmParams p)
 {
-    using R = Ring<PAIR>;
+    using R = Ring<PAIR, LDG>;
     constexpr int STAGES = R::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -435,7 +670,10 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * STAGES + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * STAGES + 5) + 4);
-    static_assert(8 * (2 * STAGES + 5) + 8 <= kBarBytes, "barrier area");
+    // loader form: the issuer threads' arrivals (and the completion of their copies) of a slice
+    auto copied_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 6 + s); };
+    const uint32_t side0 = bar0 + kBarBytes;  // STAGES x kSideBytes (loader form)
+    static_assert(8 * (3 * STAGES + 6) <= kBarBytes, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -448,9 +686,13 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     constexpr int kEpiArrivals = PAIR ? 8 : 4;  // one per epilogue warp of every CTA
 
     if (threadIdx.x == 0) {
+        // the arming arrival of rank 0's producer, and with loader warps one arrival of the
+        // fixer warps of each CTA once the loaders' part of the slice is in place
+        constexpr uint32_t kFullArrivals = LDG ? 1u + (PAIR ? 2u : 1u) : 1u;
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);   // the arming arrival of rank 0's producer
+            mbar_init(full_bar(s), kFullArrivals);
             mbar_init(empty_bar(s), 1);  // the MMA issuer's commit
+            if (LDG) mbar_init(copied_bar(s), 2 * kIssuers);  // an arrival and a copy completion each
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -459,10 +701,12 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(&map_b);
-        tma_prefetch_desc(&map_b_half);
-        tma_prefetch_desc(&map_b_quarter);
+        if (!(LDG && p.a_ldg)) tma_prefetch_desc(&map_a);
+        if (!(LDG && p.b_ldg)) {
+            tma_prefetch_desc(&map_b);
+            tma_prefetch_desc(&map_b_half);
+            tma_prefetch_desc(&map_b_quarter);
+        }
     }
     // A pair allocates TMEM together, so the peer must be running; its barriers must also
     // exist before the other CTA's copies, commits and arrivals reach them.
@@ -498,8 +742,11 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 // a pair's CTA loads B columns [n0, n0 + bw) of the unit
                 const int bw = PAIR ? width / 2 : width;
                 const int32_t n0 = static_cast<int32_t>(tn * BN) + n_off + (PAIR ? int32_t(rank) * bw : 0);
-                // bytes that complete a slice on the (rank 0) full barrier: both CTAs' for a pair
-                const uint32_t bytes = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + uint32_t(bw) * BK * 2);
+                // bytes that complete a slice on the (rank 0) full barrier: both CTAs' for a
+                // pair, of the operands copied by TMA
+                const bool tma_a = !(LDG && p.a_ldg), tma_b = !(LDG && p.b_ldg);
+                const uint32_t bytes = (PAIR ? 2u : 1u) * ((tma_a ? uint32_t(A_STAGE_BYTES) : 0u) +
+                                                           (tma_b ? uint32_t(bw) * BK * 2 : 0u));
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo)) {
                         raise_abort(abort_flag);
@@ -520,17 +767,20 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                             if (PAIR) tma_load_3d_pair(dst, map, fb, c0, c1, c2);
                             else tma_load_3d(dst, map, fb, c0, c1, c2);
                         };
-                        if (A_MN) {  // A stored K x M: two 64 (m) x 64 (k) boxes
+                        if (!tma_a) {
+                        } else if (A_MN) {  // A stored K x M: two 64 (m) x 64 (k) boxes
                             load(a_dst, &map_a, m0, k0, ba);
                             load(a_dst + 8192, &map_a, m0 + 64, k0, ba);
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
                             load(a_dst, &map_a, k0, m0, ba);
                         }
-                        if (B_MN) {  // B stored K x N: bw / 64 boxes of 64 (n) x 64 (k)
+                        if (!tma_b) {
+                        } else if (B_MN) {  // B stored K x N: bw / 64 boxes of 64 (n) x 64 (k)
                             for (int j = 0; j < bw / 64; ++j) load(b_dst + 8192 * j, &map_b, n0 + 64 * j, k0, bb);
                         } else {     // B stored N x K: one 64 (k) x bw (n) box
                             load(b_dst, bw == BN ? &map_b : bw == BN / 2 ? &map_b_half : &map_b_quarter, k0, n0, bb);
                         }
+                        if (bytes == 0) filled &= ~(1u << stage);  // no copy of this CTA's in flight
                     } else {
                         filled &= ~(1u << stage);  // nothing in flight on this slot
                     }
@@ -587,7 +837,8 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, tmo)) {
+                    // the peer's loader warps complete slices by release arrivals at cluster scope
+                    if (!mbar_wait<LDG && PAIR>(full_bar(stage), phase, abort_flag, tmo)) {
                         raise_abort(abort_flag);
                         ok = false;
                         break;
@@ -623,6 +874,96 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 mbar_wait(drain_bar, 0, &no_abort, 100000000ull);
             }
         }
+    } else if (LDG && warp >= (kThreads + kIssuers) / 32) {
+        // ---------------- fixer warps (loader form): wait for a slice's copies, shift its
+        // unaligned rows into place, order the slice before the tensor cores' reads (proxy
+        // fence; these threads have no copies of their own in flight) and announce it.
+        const int tf = threadIdx.x - (kThreads + kIssuers);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
+            const Unit x = decode_unit(p, u);
+            int64_t tm, tn;
+            const int64_t bt = x.t / p.per_batch;
+            raster(x.t - bt * p.per_batch, rows_r, p.tiles_n, p.log_group, tm, tn);
+            if (PAIR) tm = 2 * tm + rank;
+            const int bw = PAIR ? x.width / 2 : x.width;
+            const int64_t m0 = tm * BM;
+            const int64_t n0 = tn * BN + x.n_off + (PAIR ? int64_t(rank) * bw : 0);
+            const uint16_t *a_mat = p.a_ptr + (p.a_batched ? bt * p.stride_a : 0);
+            const uint16_t *b_mat = p.b_ptr + (p.b_batched ? bt * p.stride_b : 0);
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                bool got = true;
+                if (tf == 0) got = mbar_wait(copied_bar(stage), phase, abort_flag, tmo);
+                if (group_any<3, kFixers>(!got)) {
+                    if (tf == 0) raise_abort(abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int64_t k0 = int64_t(kb) * BK;
+                const uint32_t side = side0 + uint32_t(stage) * R::kSideBytes;
+                if (p.a_ldg) ldg_fix<A_MN != 0, BM>(sA + stage * A_STAGE_BYTES, side, a_mat, p.lda, p.M, p.K, m0, k0, tf);
+                if (p.b_ldg) {
+                    const uint32_t b_dst = sB + stage * R::kBStageBytes, b_side = side + BM * 16;
+                    if (bw == 256) ldg_fix<B_MN != 0, 256>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, tf);
+                    else if (bw == 128) ldg_fix<B_MN != 0, 128>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, tf);
+                    else ldg_fix<B_MN != 0, 64>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, tf);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("bar.sync 3, %0;" ::"n"(kFixers) : "memory");
+                if (tf == 0) {
+                    if (PAIR) mbar_arrive_cluster(map_to_rank(full_bar(stage), 0));
+                    else mbar_arrive(full_bar(stage));
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (LDG && warp >= kThreads / 32) {
+        // ---------------- issuer warps (loader form): copy each slice once its slot is free;
+        // the copies complete on the slot's copied barrier, so these warps never wait for them.
+        const int ti = threadIdx.x - kThreads;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t u = unit0; u < p.num_units; u += ustride) {
+            const Unit x = decode_unit(p, u);
+            int64_t tm, tn;
+            const int64_t bt = x.t / p.per_batch;
+            raster(x.t - bt * p.per_batch, rows_r, p.tiles_n, p.log_group, tm, tn);
+            if (PAIR) tm = 2 * tm + rank;
+            const int bw = PAIR ? x.width / 2 : x.width;
+            const int64_t m0 = tm * BM;
+            const int64_t n0 = tn * BN + x.n_off + (PAIR ? int64_t(rank) * bw : 0);
+            const uint16_t *a_mat = p.a_ptr + (p.a_batched ? bt * p.stride_a : 0);
+            const uint16_t *b_mat = p.b_ptr + (p.b_batched ? bt * p.stride_b : 0);
+            bool ok = true;
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                bool got = true;
+                if (ti == 0) got = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, tmo);
+                if (group_any<2, kIssuers>(!got)) {
+                    if (ti == 0) raise_abort(abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int64_t k0 = int64_t(kb) * BK;
+                const uint32_t side = side0 + uint32_t(stage) * R::kSideBytes;
+                if (p.a_ldg) ldg_issue<A_MN != 0, BM>(sA + stage * A_STAGE_BYTES, side, a_mat, p.lda, p.M, p.K, m0, k0, ti);
+                if (p.b_ldg) {
+                    const uint32_t b_dst = sB + stage * R::kBStageBytes, b_side = side + BM * 16;
+                    if (bw == 256) ldg_issue<B_MN != 0, 256>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, ti);
+                    else if (bw == 128) ldg_issue<B_MN != 0, 128>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, ti);
+                    else ldg_issue<B_MN != 0, 64>(b_dst, b_side, b_mat, p.ldb, p.N, p.K, n0, k0, ti);
+                }
+                // one arrival when this thread's copies have landed, one now (release of the
+                // element-wise stores above)
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(copied_bar(stage)) : "memory");
+                mbar_arrive(copied_bar(stage));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+        }
+        // no copy may land after the CTA's shared memory is gone
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     } else {
         // ---------------- epilogue (warps 2..5; TMEM lane quarter = warp % 4)
         const int quarter = warp & 3;
@@ -844,7 +1185,7 @@ struct Maps {
 };
 
 // Largest number of two-CTA clusters of the pair kernel that can be resident at once (0: none).
-template <int A_MN, int B_MN>
+template <int A_MN, int B_MN, bool LDG>
 int max_pair_clusters(int dev_id)
 {
     static std::atomic<int> cached[64];
@@ -853,8 +1194,8 @@ int max_pair_clusters(int dev_id)
     if (known.load(std::memory_order_acquire) & bit) return cached[dev_id & 63].load();
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
+    cfg.blockDim = dim3(threads_of<LDG>(), 1, 1);
+    cfg.dynamicSmemBytes = Ring<true, LDG>::kSmemBytes;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -863,7 +1204,7 @@ int max_pair_clusters(int dev_id)
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tcgen05_kernel<A_MN, B_MN, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tcgen05_kernel<A_MN, B_MN, true, LDG>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -872,20 +1213,21 @@ int max_pair_clusters(int dev_id)
     return n;
 }
 
-template <int A_MN, int B_MN, bool PAIR>
+template <int A_MN, int B_MN, bool PAIR, bool LDG>
 cudaError_t set_smem_attr(int dev_id)
 {
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = uint64_t(1) << (dev_id & 63);
     if (attr_set.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, PAIR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<PAIR>::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, PAIR, LDG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ring<PAIR, LDG>::kSmemBytes);
     if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_release);
     return e;
 }
 
 // Plans the unit schedule and launches.  With pairs, units are tile pairs along M.
-template <int A_MN, int B_MN>
+template <int A_MN, int B_MN, bool LDG>
 cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaStream_t stream)
 {
     // GEMM_GB300_HGEMM_PAIR=0: one CTA per tile even where pairs would be used
@@ -896,8 +1238,8 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     bool pair = p.tiles_m >= 2 && !(pair_env && pair_env[0] == '0');
     int max_clusters = 0;
     if (pair) {
-        if (set_smem_attr<A_MN, B_MN, true>(dev.device) != cudaSuccess) return cudaGetLastError();
-        max_clusters = max_pair_clusters<A_MN, B_MN>(dev.device);
+        if (set_smem_attr<A_MN, B_MN, true, LDG>(dev.device) != cudaSuccess) return cudaGetLastError();
+        max_clusters = max_pair_clusters<A_MN, B_MN, LDG>(dev.device);
         pair = max_clusters > 0;
     }
     // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
@@ -928,19 +1270,19 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         p.num_units = full + 2 * tail;
     }
     if (!pair) {
-        cudaError_t e = set_smem_attr<A_MN, B_MN, false>(dev.device);
+        cudaError_t e = set_smem_attr<A_MN, B_MN, false, LDG>(dev.device);
         if (e != cudaSuccess) return e;
-        hgemm_tcgen05_kernel<A_MN, B_MN, false>
-            <<<static_cast<unsigned>(workers), kThreads, Ring<false>::kSmemBytes, stream>>>(m.a, m.b, m.b_half,
-                                                                                           m.b_quarter, p);
+        hgemm_tcgen05_kernel<A_MN, B_MN, false, LDG>
+            <<<static_cast<unsigned>(workers), threads_of<LDG>(), Ring<false, LDG>::kSmemBytes, stream>>>(
+                m.a, m.b, m.b_half, m.b_quarter, p);
         const cudaError_t le = cudaGetLastError();
         if (le == cudaSuccess) count_launches();
         return le;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * workers), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
+    cfg.blockDim = dim3(threads_of<LDG>(), 1, 1);
+    cfg.dynamicSmemBytes = Ring<true, LDG>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -949,7 +1291,7 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true>, m.a, m.b, m.b_half,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true, LDG>, m.a, m.b, m.b_half,
                                              m.b_quarter, p);
     if (e == cudaSuccess) count_launches();
     return e;
@@ -966,11 +1308,21 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     const int a_mn = opA == GEMM_OP_T;  // A stored K x M
     const int b_mn = opB == GEMM_OP_N;  // B stored K x N
     const int bf = dtype == kInBf16;
+    // An operand TMA can read: 16-byte aligned base, leading dimension and batch stride
+    // multiples of 8 elements (16 bytes).  Any other 2-byte aligned operand goes through the
+    // loader warps (odd byte addresses are refused before this point).
+    auto tma_ok = [&](const void *ptr, int64_t ld, int64_t stride) {
+        return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 8 == 0 && (batch <= 1 || stride % 8 == 0);
+    };
+    const bool a_ldg = !tma_ok(A, lda, strideA), b_ldg = !tma_ok(B, ldb, strideB);
     Maps m;
-    const bool ok_a = a_mn ? make_map(&m.a, A, K, M, lda, 64, BK, batch, strideA, bf)
-                           : make_map(&m.a, A, M, K, lda, BK, BM, batch, strideA, bf);
-    bool ok_b;
-    if (b_mn) {  // 64 (n) x 64 (k) boxes serve every unit width
+    std::memset(&m, 0, sizeof(m));
+    bool ok_a = true, ok_b = true;
+    if (!a_ldg)
+        ok_a = a_mn ? make_map(&m.a, A, K, M, lda, 64, BK, batch, strideA, bf)
+                    : make_map(&m.a, A, M, K, lda, BK, BM, batch, strideA, bf);
+    if (b_ldg) {
+    } else if (b_mn) {  // 64 (n) x 64 (k) boxes serve every unit width
         ok_b = make_map(&m.b, B, K, N, ldb, 64, BK, batch, strideB, bf);
         m.b_half = m.b;
         m.b_quarter = m.b;
@@ -995,6 +1347,14 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     p.b_batched = batch > 1 && strideB != 0;
     p.stride_c = batch > 1 ? strideC : 0;
     p.ab_format = bf ? 1u : 0u;
+    p.a_ldg = a_ldg;
+    p.b_ldg = b_ldg;
+    p.a_ptr = A;
+    p.b_ptr = B;
+    p.lda = lda;
+    p.ldb = ldb;
+    p.stride_a = strideA;
+    p.stride_b = strideB;
     p.timeout_ns = 2000000000ull;
     p.inject_stall = 0;
     // GEMM_GB300_HGEMM_GROUP=g (sweeps only): a raster group of 2^g tile (pair) rows
@@ -1006,8 +1366,13 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
         p.timeout_ns = 20000000ull;
     }
     cudaError_t e;
-    if (a_mn) e = b_mn ? launch_t<1, 1>(dev, m, p, stream) : launch_t<1, 0>(dev, m, p, stream);
-    else e = b_mn ? launch_t<0, 1>(dev, m, p, stream) : launch_t<0, 0>(dev, m, p, stream);
+    if (a_ldg || b_ldg) {
+        if (a_mn) e = b_mn ? launch_t<1, 1, true>(dev, m, p, stream) : launch_t<1, 0, true>(dev, m, p, stream);
+        else e = b_mn ? launch_t<0, 1, true>(dev, m, p, stream) : launch_t<0, 0, true>(dev, m, p, stream);
+    } else {
+        if (a_mn) e = b_mn ? launch_t<1, 1, false>(dev, m, p, stream) : launch_t<1, 0, false>(dev, m, p, stream);
+        else e = b_mn ? launch_t<0, 1, false>(dev, m, p, stream) : launch_t<0, 0, false>(dev, m, p, stream);
+    }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 

@@ -1,12 +1,5 @@
-// Operand re-layout into per-stream scratch: packing of 16-bit operands whose layout the
-// tensor-memory-access unit cannot read, and transposition of K-contiguous fp32 operands.
-//
-// TMA needs a 16-byte aligned base and row (and batch) strides that are multiples of 16
-// bytes.  An fp16 / bf16 operand with an odd leading dimension, an unaligned base or an
-// unaligned batch stride is first copied by pack_rows_u16 into a scratch buffer with the
-// leading dimension rounded up to 8 elements, then read from there.  The copy moves
-// 2 bytes per element in each direction, which is small next to the 2*M*N*K flops of any
-// GEMM large enough to care.
+// Operand re-layout into per-stream scratch: transposition of K-contiguous fp32 operands,
+// so that the SGEMM kernel reads both operands as 16-byte [k][x] rows.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -18,33 +11,7 @@
 namespace gemm {
 namespace {
 
-// dst[b][r][c] = src[b][r][c] for c < cols, 0 for cols <= c < ldp (the row padding).
-// Each thread writes one aligned 16-byte group of 8 elements.
-__global__ void pack_rows_u16(const uint16_t *__restrict__ src, int64_t ld, int64_t stride,
-                              uint16_t *__restrict__ dst, int64_t ldp, int64_t rows, int64_t cols,
-                              int64_t batch)
-{
-    const int64_t groups_per_row = ldp / 8;
-    const int64_t total = batch * rows * groups_per_row;
-    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < total;
-         g += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t cg = g % groups_per_row;
-        const int64_t rb = g / groups_per_row;
-        const int64_t r = rb % rows, b = rb / rows;
-        const uint16_t *s = src + b * stride + r * ld + cg * 8;
-        uint16_t v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = cg * 8 + e < cols ? s[e] : uint16_t(0);
-        uint4 w;
-        w.x = uint32_t(v[0]) | (uint32_t(v[1]) << 16);
-        w.y = uint32_t(v[2]) | (uint32_t(v[3]) << 16);
-        w.z = uint32_t(v[4]) | (uint32_t(v[5]) << 16);
-        w.w = uint32_t(v[6]) | (uint32_t(v[7]) << 16);
-        *reinterpret_cast<uint4 *>(dst + (b * rows + r) * ldp + cg * 8) = w;
-    }
-}
-
-// One growable scratch buffer per (device, stream) for re-laid-out operands A and B.
+// One growable scratch buffer per (device, stream) for transposed operands A and B.
 struct PackBuffers {
     void *ptr[2] = {nullptr, nullptr};
     size_t bytes[2] = {0, 0};
@@ -138,28 +105,6 @@ bool transpose_f32_operand(int dev, cudaStream_t stream, int which, const float 
     *out = dst;
     *ld_out = ldt;
     *stride_out = stride == 0 ? 0 : cols * ldt;
-    return true;
-}
-
-bool pack_u16_operand(int dev, cudaStream_t stream, int which, const uint16_t *src, int64_t rows,
-                      int64_t cols, int64_t ld, int64_t stride, int64_t batch, const uint16_t **out,
-                      int64_t *ld_out, int64_t *stride_out)
-{
-    const int64_t ldp = (cols + 7) / 8 * 8;
-    const int64_t nb = stride == 0 ? 1 : batch;  // a shared operand is packed once
-    const size_t bytes = size_t(nb) * size_t(rows) * size_t(ldp) * 2;
-    uint16_t *dst = static_cast<uint16_t *>(pack_buffer(dev, stream, which, bytes > 0 ? bytes : 16));
-    if (dst == nullptr) return false;
-    const int64_t total = nb * rows * (ldp / 8);
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 65536) blocks = 65536;
-    if (blocks < 1) blocks = 1;
-    pack_rows_u16<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld, stride, dst, ldp, rows, cols, nb);
-    if (cudaGetLastError() != cudaSuccess) return false;
-    count_launches();
-    *out = dst;
-    *ld_out = ldp;
-    *stride_out = stride == 0 ? 0 : rows * ldp;
     return true;
 }
 

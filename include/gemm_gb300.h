@@ -24,11 +24,11 @@
  * Ownership.  A, B and C are device memory owned by the caller (host memory for the
  * *_host entry points); the library never frees or retains them.  C must not overlap A or
  * B.  The library keeps scratch per (device, stream): a split-K workspace (64 MB and 8192
- * counters), two operand buffers for re-laid-out operands and, for the *_host entry points,
- * a staging area; each is allocated when first needed, grown when a larger problem needs
- * it (after the stream's earlier work), kept until exit, and never allocated while the
- * stream is being captured (a call then takes a path that needs no new scratch, except
- * where a 16-bit operand must be packed -- see gemm_hgemm_f16f32 -- or host matrices staged).
+ * counters), two buffers for transposed fp32 operands and, for the *_host entry points, a
+ * staging area; each is allocated when first needed, grown when a larger problem needs it
+ * (after the stream's earlier work), kept until exit, and never allocated while the stream
+ * is being captured (a call then takes a path that needs no new scratch, except where host
+ * matrices must be staged).
  *
  * Asynchrony.  A call validates its arguments on the host, launches on `stream` (a
  * cudaStream_t passed as void*; NULL means the legacy default stream of the current
@@ -92,12 +92,12 @@ GEMM_API gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, i
  * (the mixed-precision mode of the copecc "GEMM" page, section "Batched 执行与混合精度", and
  * of the dandandamowang.xyz "GEMM优化（二）" page): products of IEEE binary16 inputs are
  * summed in fp32, then C = alpha * sum + beta * C in fp32.
- * A, B: IEEE binary16 bit patterns (uint16_t), 2-byte aligned, any lda, ldb.  The
- * tensor-memory-access unit reads 16-byte granules, so an operand whose base is not 16-byte
- * aligned or whose lda (ldb) is not a multiple of 8 elements is first copied into a scratch
- * buffer of this stream with the leading dimension rounded up (the buffer is allocated on
- * first need, grows when a larger operand needs it, and is kept until exit; during stream
- * capture no buffer can be allocated and such an operand gives GEMM_ERR_MISALIGNED).
+ * A, B: IEEE binary16 bit patterns (uint16_t), 2-byte aligned, any lda, ldb; an odd byte
+ * address gives GEMM_ERR_MISALIGNED.  The tensor-memory-access unit reads rows only from a
+ * 16-byte aligned base with a leading dimension that is a multiple of 8 elements; an operand
+ * laid out otherwise is read by four loader warps of the same kernel instead (cp.async
+ * copies where its rows are 4-byte aligned, loads through registers where they are only
+ * 2-byte aligned), with no extra launch and no scratch memory.
  * C: fp32, 4-byte aligned, any ldc.
  * Limits: M, N, K < 2^31; lda, ldb < 2^35 elements.
  */
@@ -125,8 +125,8 @@ GEMM_API gemm_status_t gemm_bgemm_bf16f32(gemm_op_t opA, gemm_op_t opB, int64_t 
  * with the row-major rules of the single calls.  A stride of 0 shares that operand between
  * all problems; strideC must keep the outputs apart: strideC >= (M - 1) * ldc + N when
  * batch > 1 (else GEMM_ERR_INVALID_VALUE).  batch == 0 launches nothing.  A 16-bit
- * operand whose batch stride is not a multiple of 8 elements is packed like an unaligned
- * leading dimension (see gemm_hgemm_f16f32).
+ * operand whose batch stride is not a multiple of 8 elements is read by the loader warps,
+ * like one with an unaligned leading dimension (see gemm_hgemm_f16f32).
  * Limits: batch <= 2^31.
  */
 GEMM_API gemm_status_t gemm_sgemm_f32_strided_batched(gemm_op_t opA, gemm_op_t opB, int64_t M,

@@ -136,7 +136,7 @@ def test_tensor_core_strided_batched(dtype, opA, opB):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_tensor_core_strided_batched_unaligned_strides_are_packed(dtype):
+def test_tensor_core_strided_batched_unaligned_strides_through_the_loader(dtype):
     c = _batched_case(dtype, 3, 200, 136, 100, "N", "T", seed=6)
     # shift every problem's operands by an odd number of elements
     c["sA"] += 3

@@ -111,29 +111,6 @@ def test_linear_layer_opBT_beta1_full_oracle():
     parity.check_full(w, inputs, dev["C"])
 
 
-@pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_unaligned_operands_are_packed(opA, opB, dtype):
-    # odd leading dimensions and bases one element off a 16-byte boundary: the library packs
-    # A and B into aligned scratch copies before the tensor-memory-access loads
-    M, N, K = 300, 270, 333
-    w = workloads.Workload(f"unaligned_{dtype}_{opA}{opB}", dtype, M, N, K, opA, opB,
-                           alpha=0.75, beta=0.25, seed=51, pad=(3, 5, 1))
-    inputs = workloads.make_inputs(w)
-    A = torch.zeros(inputs["A"].numel() + 1, dtype=inputs["A"].dtype)
-    B = torch.zeros(inputs["B"].numel() + 1, dtype=inputs["B"].dtype)
-    A[1:] = inputs["A"].reshape(-1)
-    B[1:] = inputs["B"].reshape(-1)
-    dA, dB, dC = A.cuda(), B.cuda(), inputs["C"].cuda()
-    fn = gemm_hgemm_f16f32 if dtype == "f16" else g.gemm_bgemm_bf16f32
-    for _ in range(2):  # the second call reuses the stream's pack buffers
-        dC.copy_(inputs["C"])
-        fn(opA, opB, M, N, K, w.alpha, dA[1:], w.lda, dB[1:], w.ldb, w.beta, dC, w.ldc)
-        torch.cuda.synchronize()
-        assert gemm_get_device_status() == 0
-        parity.check_full(w, inputs, dC[:, : w.N].contiguous())
-
-
 def test_odd_byte_addresses_are_refused():
     A = torch.zeros(64, 72, dtype=torch.float16, device="cuda")
     C = torch.zeros(64, 64, device="cuda")
