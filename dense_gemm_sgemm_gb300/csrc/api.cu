@@ -171,6 +171,8 @@ static gemm_status_t host_impl(int opA, int opB, int64_t M, int64_t N, int64_t K
     const size_t bA = up(size_t(nA) * sizeof(T)), bB = up(size_t(nB) * sizeof(T));
     const size_t bC = up(size_t(nC) * sizeof(float));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // held until this call's copies and kernels are enqueued (see host_staging)
+    std::lock_guard<std::mutex> lk(host_call_mutex());
     char *base = static_cast<char *>(host_staging(dev.device, st, bA + bB + bC));
     if (base == nullptr) return GEMM_ERR_UNSUPPORTED;
     T *dA = reinterpret_cast<T *>(base), *dB = reinterpret_cast<T *>(base + bA);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/gemm_gb300.h"
 
 namespace gemm {
@@ -35,6 +37,13 @@ struct DeviceInfo {
 // Cached per-device properties of the current device; false if there is none.
 bool current_device(DeviceInfo &info);
 
+// Scratch kept per (device, stream) -- split-K workspace, transposition buffers, host
+// staging -- exists for at most kMaxScratchStreams streams per device and kind: a caller
+// cycling through many short-lived streams must not accumulate it without bound.  Calls on
+// further streams take the paths that need no scratch (no split-K, no transposition); the
+// host-memory entry points release the other streams' staging instead (see host_staging).
+constexpr int kMaxScratchStreams = 16;
+
 // Split-K workspace of one (device, stream): kWorkspaceBytes of partial tiles and
 // kWorkspaceCounters arrival counters that are zero between kernels.
 constexpr size_t kWorkspaceBytes = size_t(64) << 20;
@@ -43,15 +52,21 @@ struct StreamWorkspace {
     float *data = nullptr;
     unsigned int *counters = nullptr;
 };
-// False when no workspace exists and none can be allocated now (e.g. during capture).
+// False when no workspace exists and none can be allocated now (during capture, or when
+// kMaxScratchStreams other streams of the device hold one).
 bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out);
 // Zeroes the arrival counters of every workspace of device `dev` (after a kernel gave up on
 // a bounded wait and may have left counters raised).  Synchronises those streams.
 void reset_workspace_counters(int dev);
 // Device staging area of at least `bytes` for the host-memory entry points, one per
-// (device, stream), grown by reallocation after synchronising the stream.  nullptr when it
-// would have to be (re)allocated while the stream is being captured, or allocation fails.
+// (device, stream), grown by reallocation after synchronising the stream.  A new stream
+// beyond kMaxScratchStreams first synchronises the device and frees the other streams'
+// areas.  The caller holds host_call_mutex() from before this call until the call's copies
+// and kernels are enqueued, so no other host call is using an area being freed.  nullptr
+// when it would have to be (re)allocated while the stream is being captured, or allocation
+// fails.
 void *host_staging(int dev, cudaStream_t stream, size_t bytes);
+std::mutex &host_call_mutex();
 
 // Launchers (return cudaSuccess or the launch error).  Arguments are already validated.
 // A batch of `batch` problems: operand b of problem i starts `stride` elements after that

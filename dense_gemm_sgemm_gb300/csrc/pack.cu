@@ -21,10 +21,16 @@ std::map<std::pair<int, cudaStream_t>, PackBuffers> g_bufs;
 
 // A buffer of at least `bytes` for operand slot `which` (0 = A, 1 = B) of this stream.
 // Grows by reallocation (after the stream's earlier work using it has finished); never
-// allocates while the stream is being captured.
+// allocates while the stream is being captured, nor for a new stream once kMaxScratchStreams
+// streams of the device hold buffers (the caller then reads the operand untransposed).
 void *pack_buffer(int dev, cudaStream_t stream, int which, size_t bytes)
 {
     std::lock_guard<std::mutex> lk(g_mu);
+    if (g_bufs.find({dev, stream}) == g_bufs.end()) {
+        int held = 0;
+        for (const auto &kv : g_bufs) held += kv.first.first == dev;
+        if (held >= kMaxScratchStreams) return nullptr;
+    }
     PackBuffers &pb = g_bufs[{dev, stream}];
     if (pb.bytes[which] >= bytes) return pb.ptr[which];
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -170,8 +170,16 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
                          int64_t ldc, int64_t strideC, int64_t batch, cudaStream_t stream)
 {
     Plan plan = choose_plan(M, N, K, batch, dev.num_sms, true);
+    // Two splits of every 64 x 64 tile run as two-CTA clusters that hand the partial over
+    // through distributed shared memory; every other split plan needs the stream's workspace.
+    // GEMM_GB300_SGEMM_PAIR=0 keeps the workspace hand-off (for tests).
+    const char *pair_env = std::getenv("GEMM_GB300_SGEMM_PAIR");
+    const bool pair_ok = pair_env == nullptr || pair_env[0] != '0';
+    auto cluster_pair = [&](const Plan &pl) {
+        return pl.splits == 2 && pl.full_tiles == 0 && pl.cfg->name == 'S' && pair_ok;
+    };
     StreamWorkspace w;
-    if (plan.splits > 1 && !stream_workspace(dev.device, stream, w))
+    if (plan.splits > 1 && !cluster_pair(plan) && !stream_workspace(dev.device, stream, w))
         plan = choose_plan(M, N, K, batch, dev.num_sms, false);  // no workspace: plan without split
     const CfgDesc &cfg = *plan.cfg;
     if (batch <= 1) strideA = strideB = strideC = 0;
@@ -239,11 +247,8 @@ cudaError_t launch_sgemm(const DeviceInfo &dev, int opA, int opB, int64_t M, int
         }
         // Two splits of every 64 x 64 tile: the pair forms a cluster and hands its partial
         // over through distributed shared memory instead of the workspace (the same sum,
-        // p0 + p1).  GEMM_GB300_SGEMM_PAIR=0 keeps the workspace hand-off (for tests).
-        if (plan.splits == 2 && plan.full_tiles == 0 && cfg.name == 'S') {
-            const char *e = std::getenv("GEMM_GB300_SGEMM_PAIR");
-            if (e == nullptr || e[0] != '0') return launch_SP(dev.device, a_mode, b_mode, p, stream);
-        }
+        // p0 + p1).
+        if (cluster_pair(plan)) return launch_SP(dev.device, a_mode, b_mode, p, stream);
         return cfg.launch_split(dev.device, a_mode, b_mode, p, stream);
     }
     return cfg.launch(dev.device, a_mode, b_mode, p, stream);

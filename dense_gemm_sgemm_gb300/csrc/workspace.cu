@@ -3,10 +3,11 @@
 //
 // One workspace per (device, stream): calls on the same stream are ordered and may share it;
 // calls on different streams never do.  It is allocated once, on the first call on that
-// stream that splits K, kept until the process exits, and never allocated while the stream
-// is being captured (the call then runs without splitting).  Every kernel that uses the
-// arrival counters leaves them at zero when it finishes -- unless it gave up on a bounded
-// wait, after which reset_workspace_counters() restores them.
+// stream that splits K through the workspace, kept until the process exits, and never
+// allocated while the stream is being captured or once kMaxScratchStreams streams of the
+// device hold one (the call then runs without splitting).  Every kernel that uses the arrival
+// counters leaves them at zero when it finishes -- unless it gave up on a bounded wait, after
+// which reset_workspace_counters() restores them.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -36,6 +37,9 @@ bool stream_workspace(int dev, cudaStream_t stream, StreamWorkspace &out)
         cudaGetLastError();
         return false;
     }
+    int held = 0;
+    for (const auto &kv : g_ws) held += kv.first.first == dev;
+    if (held >= kMaxScratchStreams) return false;
     StreamWorkspace w;
     if (cudaMalloc(&w.data, kWorkspaceBytes) != cudaSuccess ||
         cudaMalloc(&w.counters, kWorkspaceCounters * sizeof(unsigned int)) != cudaSuccess ||
@@ -55,20 +59,42 @@ struct Staging {
     void *ptr = nullptr;
     size_t bytes = 0;
 };
-std::mutex g_stage_mu;
+std::mutex g_host_call_mu;
 std::map<std::pair<int, cudaStream_t>, Staging> g_stage;
 }  // namespace
 
+std::mutex &host_call_mutex() { return g_host_call_mu; }
+
 void *host_staging(int dev, cudaStream_t stream, size_t bytes)
 {
-    std::lock_guard<std::mutex> lk(g_stage_mu);
-    Staging &sg = g_stage[{dev, stream}];
-    if (sg.bytes >= bytes && sg.ptr) return sg.ptr;
+    auto it = g_stage.find({dev, stream});
+    if (it != g_stage.end() && it->second.bytes >= bytes && it->second.ptr) return it->second.ptr;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
         cudaGetLastError();
         return nullptr;
     }
+    if (it == g_stage.end()) {
+        int held = 0;
+        for (const auto &kv : g_stage) held += kv.first.first == dev;
+        if (held >= kMaxScratchStreams) {
+            // Every host call holds host_call_mutex() until its work is enqueued, and the
+            // device synchronisation waits for all enqueued work: no area is still in use.
+            if (cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+            for (auto jt = g_stage.begin(); jt != g_stage.end();) {
+                if (jt->first.first == dev) {
+                    cudaFree(jt->second.ptr);
+                    jt = g_stage.erase(jt);
+                } else {
+                    ++jt;
+                }
+            }
+        }
+    }
+    Staging &sg = g_stage[{dev, stream}];
     if (sg.ptr) {
         // Earlier calls on this stream may still be copying through the old area.
         if (cudaStreamSynchronize(stream) != cudaSuccess) {
@@ -98,11 +124,11 @@ uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); 
 void reset_workspace_counters(int dev)
 {
     std::lock_guard<std::mutex> lk(g_ws_mu);
+    // The whole device, not each workspace's stream: a stream may have been destroyed since.
+    cudaDeviceSynchronize();
     for (auto &kv : g_ws)
-        if (kv.first.first == dev) {
-            cudaStreamSynchronize(kv.first.second);
-            cudaMemset(kv.second.counters, 0, kWorkspaceCounters * sizeof(unsigned int));
-        }
+        if (kv.first.first == dev) cudaMemset(kv.second.counters, 0, kWorkspaceCounters * sizeof(unsigned int));
+    cudaDeviceSynchronize();
     cudaGetLastError();
 }
 

@@ -28,7 +28,11 @@
  * staging area; each is allocated when first needed, grown when a larger problem needs it
  * (after the stream's earlier work), kept until exit, and never allocated while the stream
  * is being captured (a call then takes a path that needs no new scratch, except where host
- * matrices must be staged).
+ * matrices must be staged).  At most 16 streams per device hold each kind: calls on further
+ * streams run without split-K or transposition (same results within the stated bounds,
+ * slower), and a *_host call on a further stream first synchronises the device and releases
+ * the other streams' staging areas.  The *_host calls enqueue their work one host thread at
+ * a time.
  *
  * Asynchrony.  A call validates its arguments on the host, launches on `stream` (a
  * cudaStream_t passed as void*; NULL means the legacy default stream of the current
