@@ -179,9 +179,9 @@ def csrc_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(kernel: str, profile: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are
-    unchanged since the capture."""
+def _profile_fields(kernel: str, profile: str):
+    """Fields of a committed ncu summary, if the kernel's sources are unchanged since the
+    capture (else None)."""
     path = os.path.join(ROOT, "profiles", profile)
     try:
         digest = csrc_digest(kernel)
@@ -190,10 +190,27 @@ def _traffic_from_profile(kernel: str, profile: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-        if fields.get("source_sha256_16") != digest:
-            return None
-        return float(fields["dram_bytes_per_launch"])
+        return fields if fields.get("source_sha256_16") == digest else None
     except Exception:
+        return None
+
+
+def _traffic_from_profile(kernel: str, profile: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are
+    unchanged since the capture."""
+    fields = _profile_fields(kernel, profile)
+    try:
+        return float(fields["dram_bytes_per_launch"]) if fields else None
+    except (KeyError, ValueError):
+        return None
+
+
+def _ncu_duration_us(kernel: str, profile: str):
+    """The kernel's duration under ncu (one launch, cold L2, serialised) from the same summary."""
+    fields = _profile_fields(kernel, profile)
+    try:
+        return float(fields["duration_us"]) if fields else None
+    except (KeyError, ValueError):
         return None
 
 
@@ -404,6 +421,7 @@ def run_ours(args, rank, world, local):
     kernel = "sgemm_ffma" if w.dtype == "f32" else "hgemm_tcgen05"
     peak, bound, peak_src, roof = _roofline_peak(w, peaks)
     traffic = _traffic_from_profile(kernel, f"{kernel}_{w.name}.txt")
+    ncu_us = _ncu_duration_us(kernel, f"{kernel}_{w.name}.txt")
     # The library's own FFMA-chain probe, run after the timed region: a measured FP32
     # multiply-add ceiling beside the one derived from unit counts and the maximum clock.
     probe = round(lib.gemm_measure_fp32_fma_peak(), 2) if w.dtype == "f32" else None
@@ -428,6 +446,10 @@ def run_ours(args, rank, world, local):
                      "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
                                            if w.dtype != "f32" else None),
                      "peak_fma_probe": probe,
+                     # kernel-only time from the ncu summary (cold L2, no event overhead)
+                     "ncu_kernel_us": ncu_us,
+                     "frac_kernel_only": (round(w.flops / (ncu_us * 1e-6) / 1e12 / peak, 4)
+                                          if ncu_us else None),
                      "median_ms": round(statistics.median(step_ms), 5),
                      "min_ms": round(min(step_ms), 5), "max_ms": round(max(step_ms), 5)},
         "gpu_launches": launches,

@@ -27,12 +27,15 @@ def test_traffic_is_reported_only_for_the_captured_sources(tmp_path, monkeypatch
     monkeypatch.setattr(bench, "ROOT", str(root))
     digest = bench.csrc_digest("sgemm_ffma")
     prof = root / "profiles" / "p.txt"
-    prof.write_text(f"# comment: 1\nsource_sha256_16: {digest}\ndram_bytes_per_launch: 1234\n")
+    prof.write_text(f"# comment: 1\nsource_sha256_16: {digest}\ndram_bytes_per_launch: 1234\n"
+                    "duration_us: 56.5\n")
     assert bench._traffic_from_profile("sgemm_ffma", "p.txt") == 1234.0
+    assert bench._ncu_duration_us("sgemm_ffma", "p.txt") == 56.5
     # any change to the kernel's sources makes the captured counters stale
     src = root / "dense_gemm_sgemm_gb300" / "csrc" / "sgemm_kernel.cuh"
     src.write_text(src.read_text() + "\n")
     assert bench._traffic_from_profile("sgemm_ffma", "p.txt") is None
+    assert bench._ncu_duration_us("sgemm_ffma", "p.txt") is None
     # the other kernel's digest does not depend on the SGEMM sources
     assert bench.csrc_digest("hgemm_tcgen05") != bench.csrc_digest("sgemm_ffma")
     assert bench._traffic_from_profile("sgemm_ffma", "missing.txt") is None
