@@ -30,6 +30,11 @@
 // both CTAs.  PAIR = false: one CTA computes a 128 x 256 tile with cta_group::1 MMAs from
 // a 4-stage ring of 48 KB stages.
 //
+// WIDE (pairs, large problems with beta = 0): 256 x 512 pair tiles, two N = 256 MMAs per K
+// step into one 512-column accumulator per CTA; each CTA loads 256 of the B columns (4 stages
+// of 48 KB).  A quarter fewer bytes cross from L2 per flop -- the measured limit of the 256 x
+// 256 tiles -- at the price of each tile's epilogue no longer overlapping the next tile's MMAs.
+//
 // The last, partial wave of tiles is split so that more SMs share it: into K halves whose
 // fp32 partial sums are exchanged (each half finishes half of the tile's columns), or into
 // N halves.
@@ -76,17 +81,20 @@ constexpr int kLogGroup = 3;  // default raster group: 2^3 tile rows (or tile-pa
 // not 16-byte aligned), and fewer stages: its copies pass through the L1 data array, whose
 // size -- what the shared-memory carve-out leaves of the 256 KB -- bounds the bytes they can
 // have in flight (4 stages of a pair: 164 KB carve-out, 92 KB of L1).
-template <bool PAIR, bool LDG = false>
+// WIDE (pairs only): 256 x 512 pair tiles, each CTA holding 256 of the 512 B columns, 4 stages
+// of 48 KB.
+template <bool PAIR, bool LDG = false, bool WIDE = false>
 struct Ring {
-    static constexpr int kStages = LDG ? (PAIR ? 4 : 3) : (PAIR ? 6 : 4);
-    static constexpr int kBRows = PAIR ? BN / 2 : BN;
+    static constexpr int kStages = WIDE ? 4 : LDG ? (PAIR ? 4 : 3) : (PAIR ? 6 : 4);
+    static constexpr int kBRows = WIDE ? BN : PAIR ? BN / 2 : BN;
     static constexpr int kBStageBytes = kBRows * BK * 2;  // 16 KB or 32 KB
     static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
     static constexpr int kSideBytes = LDG ? (BM + kBRows) * 16 : 0;  // per stage
     static constexpr int kSmemBytes =
         kStages * (kStageBytes + kSideBytes) + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
 };
-static_assert(Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024 &&
+static_assert(Ring<true, false, true>::kSmemBytes <= 227 * 1024 &&
+                  Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024 &&
                   Ring<true, true>::kSmemBytes <= 227 * 1024 && Ring<false, true>::kSmemBytes <= 227 * 1024,
               "one CTA per SM within the 227 KB opt-in limit");
 template <bool LDG>
@@ -126,6 +134,7 @@ struct HgemmParams {
     int64_t stride_c;          // elements between consecutive C matrices
     uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
     int log_group;             // raster group of 2^log_group tile (pair) rows
+    int tile_n;                // columns of a tile: 256, or 512 for the wide pair tiles
     // Operands the tensor-memory-access unit cannot read (base not 16-byte aligned, leading
     // dimension or batch stride not a multiple of 8 elements) are read by the loader warps:
     // pointer, leading dimension and batch stride of the stored matrix, in elements.
@@ -145,7 +154,7 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const HgemmParams &p, int64_t u)
 {
-    Unit x{u, -1, 0, BN, 0, p.num_kb, -1};
+    Unit x{u, -1, 0, p.tile_n, 0, p.num_kb, -1};
     if (u >= p.full_tiles && p.tail_mode != kTailNone) {
         const int64_t r = u - p.full_tiles;
         const int h = static_cast<int>(r & 1);
@@ -412,6 +421,20 @@ __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane (one load round trip).
+__device__ __forceinline__ void tmem_ld_64(uint32_t taddr, float (&v)[64])
+{
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Shared-memory matrix descriptor of a tcgen05 operand tile stored with the 128-byte
 // swizzle (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
 //   bits  0-13 start address >> 4       bits 16-29 leading byte offset >> 4
@@ -644,13 +667,18 @@ __device__ __forceinline__ void ldg_fix(uint32_t dst, uint32_t side, const uint1
 // pair's MMAs.  LDG = true: four more warps (6-9) load the operands flagged a_ldg / b_ldg
 // into the ring themselves and warp 10 relays their slices to the MMA issuer; the producer
 // warp still arms each slice and copies the other operand (if any) by TMA.
-template <int A_MN, int B_MN, bool PAIR, bool LDG>
+template <int A_MN, int B_MN, bool PAIR, bool LDG, bool WIDE = false>
 __global__ void __launch_bounds__(threads_of<LDG>(), 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_b_half,
                      const __grid_constant__ CUtensorMap map_b_quarter, const HgemmParams p)
 {
-    using R = Ring<PAIR, LDG>;
+    static_assert(!WIDE || (PAIR && !LDG), "wide tiles: pairs of TMA-read operands");
+    using R = Ring<PAIR, LDG, WIDE>;
+    // WIDE: one 512-column accumulator (no double buffer: a tile's epilogue runs before the
+    // next tile's MMAs), two N = 256 MMAs per K step
+    constexpr int kAccs = WIDE ? 1 : 2;
+    constexpr int kAccColsT = WIDE ? 2 * BN : kAccCols;
     constexpr int STAGES = R::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -774,7 +802,17 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         } else {     // A stored M x K: one 64 (k) x 128 (m) box
                             load(a_dst, &map_a, k0, m0, ba);
                         }
-                        if (!tma_b) {
+                        if (WIDE) {  // pieces h of 128 columns at tile columns 256 h + 128 rank
+                            for (int h = 0; h < 2; ++h) {
+                                const int32_t nb = static_cast<int32_t>(tn * (2 * BN)) + 256 * h + 128 * int32_t(rank);
+                                if (B_MN) {
+                                    load(b_dst + 16384 * h, &map_b, nb, k0, bb);
+                                    load(b_dst + 16384 * h + 8192, &map_b, nb + 64, k0, bb);
+                                } else {
+                                    load(b_dst + 16384 * h, &map_b_half, k0, nb, bb);
+                                }
+                            }
+                        } else if (!tma_b) {
                         } else if (B_MN) {  // B stored K x N: bw / 64 boxes of 64 (n) x 64 (k)
                             for (int j = 0; j < bw / 64; ++j) load(b_dst + 8192 * j, &map_b, n0 + 64 * j, k0, bb);
                         } else {     // B stored N x K: one 64 (k) x bw (n) box
@@ -829,13 +867,13 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             bool ok = true, issued = false;
             for (int64_t u = unit0; ok && u < p.num_units; u += ustride) {
                 const Unit x = decode_unit(p, u);
-                const uint32_t idesc = x.width == BN ? idesc_full : idesc_half;
+                const uint32_t idesc = (WIDE || x.width == BN) ? idesc_full : idesc_half;
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, tmo)) {
                     raise_abort(abort_flag);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+                const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccColsT);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     // the peer's loader warps complete slices by release arrivals at cluster scope
                     if (!mbar_wait<LDG && PAIR>(full_bar(stage), phase, abort_flag, tmo)) {
@@ -852,9 +890,13 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                         // MN-major: step 16 rows of 128 bytes.
                         const uint64_t ad = A_MN ? smem_desc(a_tile + k * 2048, 8192, 1024)
                                                  : smem_desc(a_tile + k * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc(b_tile + k * 2048, 8192, 1024)
-                                                 : smem_desc(b_tile + k * 32, 16, 1024);
-                        umma_f16<PAIR>(d_tmem, ad, bd, idesc, (kb > x.kb0 || k > 0) ? 1u : 0u);
+                        const uint32_t accumulate = (kb > x.kb0 || k > 0) ? 1u : 0u;
+#pragma unroll
+                        for (int h = 0; h < (WIDE ? 2 : 1); ++h) {  // WIDE: the two 256-column halves
+                            const uint32_t bt = b_tile + 16384u * h;
+                            const uint64_t bd = B_MN ? smem_desc(bt + k * 2048, 8192, 1024) : smem_desc(bt + k * 32, 16, 1024);
+                            umma_f16<PAIR>(d_tmem + 256u * h, ad, bd, idesc, accumulate);
+                        }
                     }
                     issued = true;
                     // the slot is free once these MMAs have read it (a pair: in both CTAs)
@@ -865,7 +907,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 if (!ok) break;
                 umma_commit<PAIR>(accf_bar(acc));  // accumulator complete
                 if (PAIR) umma_commit<PAIR>(map_to_rank(accf_bar(acc), 1));
-                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                if (++acc == kAccs) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok && issued) {
                 // Wait for the MMAs in flight before TMEM is released.
@@ -986,15 +1028,15 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccCols);
+            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kAccColsT);
             // C = alpha * acc + beta * C for chunk c (32 columns) of the warp's 32 rows; v holds
             // this lane's row.  The rows go through the warp's staging tile (16-byte chunks
             // XOR-swizzled by row: conflict-free both ways), so that each store instruction
             // writes four 128-byte row segments instead of 32 scattered 16-byte pieces.
             float4 *tile = epi_tiles + quarter * 256;
             const int64_t row0 = tm * BM + quarter * 32;  // first row of this warp
-            auto store_chunk = [&](int c, float (&v)[32]) {
-                const int64_t gn0 = tn * BN + n_off + c * 32;
+            auto store_chunk = [&](int c, const float *v) {
+                const int64_t gn0 = tn * p.tile_n + n_off + c * 32;
                 if (gn0 >= p.N) return;  // the same for the whole warp
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -1040,13 +1082,24 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 }
                 __syncwarp();  // the tile is read before the next chunk overwrites it
             };
-            if (x.khalf < 0) {
+            if (x.khalf < 0 && LDG) {
 #pragma unroll 1
                 for (int c = 0; c < width / 32; ++c) {
                     float v[32];
                     __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the predicated stores
                     tmem_ld_32(taddr + c * 32, v);
                     store_chunk(c, v);
+                }
+            } else if (x.khalf < 0) {
+                // 64 columns per TMEM load round trip (every unit width is a multiple of 64; the
+                // loader form, limited to 168 registers a thread, keeps 32)
+#pragma unroll 1
+                for (int c = 0; c < width / 32; c += 2) {
+                    float v[64];
+                    __syncwarp();
+                    tmem_ld_64(taddr + c * 32, v);
+                    store_chunk(c, v);
+                    store_chunk(c + 1, v + 32);
                 }
             } else {
                 // K half h finishes columns [128 h, 128 h + 128) of the tile.  It publishes
@@ -1129,7 +1182,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
                 if (PAIR) mbar_arrive_cluster(map_to_rank(acce_bar(acc), 0));
                 else mbar_arrive(acce_bar(acc));
             }
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == kAccs) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
@@ -1185,7 +1238,7 @@ struct Maps {
 };
 
 // Largest number of two-CTA clusters of the pair kernel that can be resident at once (0: none).
-template <int A_MN, int B_MN, bool LDG>
+template <int A_MN, int B_MN, bool LDG, bool WIDE = false>
 int max_pair_clusters(int dev_id)
 {
     static std::atomic<int> cached[64];
@@ -1195,7 +1248,7 @@ int max_pair_clusters(int dev_id)
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(threads_of<LDG>(), 1, 1);
-    cfg.dynamicSmemBytes = Ring<true, LDG>::kSmemBytes;
+    cfg.dynamicSmemBytes = Ring<true, LDG, WIDE>::kSmemBytes;
     cudaLaunchAttribute attr{};
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -1204,7 +1257,7 @@ int max_pair_clusters(int dev_id)
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tcgen05_kernel<A_MN, B_MN, true, LDG>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tcgen05_kernel<A_MN, B_MN, true, LDG, WIDE>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -1213,15 +1266,15 @@ int max_pair_clusters(int dev_id)
     return n;
 }
 
-template <int A_MN, int B_MN, bool PAIR, bool LDG>
+template <int A_MN, int B_MN, bool PAIR, bool LDG, bool WIDE = false>
 cudaError_t set_smem_attr(int dev_id)
 {
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = uint64_t(1) << (dev_id & 63);
     if (attr_set.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, PAIR, LDG>,
+    cudaError_t e = cudaFuncSetAttribute(hgemm_tcgen05_kernel<A_MN, B_MN, PAIR, LDG, WIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ring<PAIR, LDG>::kSmemBytes);
+                                         Ring<PAIR, LDG, WIDE>::kSmemBytes);
     if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_release);
     return e;
 }
@@ -1241,6 +1294,49 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         if (set_smem_attr<A_MN, B_MN, true, LDG>(dev.device) != cudaSuccess) return cudaGetLastError();
         max_clusters = max_pair_clusters<A_MN, B_MN, LDG>(dev.device);
         pair = max_clusters > 0;
+    }
+    // Wide pair tiles (256 x 512): a quarter less L2-to-SM traffic per flop, but the single
+    // 512-column accumulator leaves each tile's epilogue exposed.  Used when the problem has
+    // at least three full waves of them and beta == 0 (an epilogue that also reads C costs
+    // more than the saving: 16384 x 4096 x 4096 with beta = 1 ran 21% slower, 8192^3 with
+    // beta = 0 2-3.5% faster); GEMM_GB300_HGEMM_WIDE=0 never, =1 whenever pairs are used (for
+    // tests).
+    if (!LDG && pair && p.tile_n == BN) {
+        const char *wide_env = std::getenv("GEMM_GB300_HGEMM_WIDE");
+        const char want = wide_env && wide_env[0] ? wide_env[0] : 'a';
+        const int64_t per_batch_w = ((p.tiles_m + 1) / 2) * ((p.N + 2 * BN - 1) / (2 * BN));
+        const int64_t work_w = per_batch_w * p.batch;
+        if (want != '0' && (want == '1' || (p.beta == 0.0f && work_w >= 3 * int64_t(max_clusters))) &&
+            set_smem_attr<A_MN, B_MN, true, false, true>(dev.device) == cudaSuccess) {
+            const int max_w = max_pair_clusters<A_MN, B_MN, false, true>(dev.device);
+            if (max_w > 0) {
+                p.tile_n = 2 * BN;
+                p.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
+                p.per_batch = per_batch_w;
+                p.full_tiles = work_w;
+                p.num_units = work_w;
+                p.tail_mode = kTailNone;
+                const int64_t clusters = work_w < max_w ? work_w : max_w;
+                cudaLaunchConfig_t cfg{};
+                cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+                cfg.blockDim = dim3(kThreads, 1, 1);
+                cfg.dynamicSmemBytes = Ring<true, false, true>::kSmemBytes;
+                cfg.stream = stream;
+                cudaLaunchAttribute attr{};
+                attr.id = cudaLaunchAttributeClusterDimension;
+                attr.val.clusterDim.x = 2;
+                attr.val.clusterDim.y = 1;
+                attr.val.clusterDim.z = 1;
+                cfg.attrs = &attr;
+                cfg.numAttrs = 1;
+                const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true, false, true>, m.a,
+                                                         m.b, m.b_half, m.b_quarter, p);
+                if (e == cudaSuccess) count_launches();
+                return e;
+            }
+        } else {
+            cudaGetLastError();
+        }
     }
     // Whole tiles (or pairs) for the full waves; when the last wave would leave more than
     // half of the workers idle, its tiles are split in two units each: K halves when there
@@ -1347,6 +1443,7 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     p.b_batched = batch > 1 && strideB != 0;
     p.stride_c = batch > 1 ? strideC : 0;
     p.ab_format = bf ? 1u : 0u;
+    p.tile_n = BN;
     p.a_ldg = a_ldg;
     p.b_ldg = b_ldg;
     p.a_ptr = A;
