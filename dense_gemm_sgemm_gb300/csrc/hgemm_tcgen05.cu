@@ -30,10 +30,12 @@
 // both CTAs.  PAIR = false: one CTA computes a 128 x 256 tile with cta_group::1 MMAs from
 // a 4-stage ring of 48 KB stages.
 //
-// WIDE (pairs, large problems with beta = 0): 256 x 512 pair tiles, two N = 256 MMAs per K
-// step into one 512-column accumulator per CTA; each CTA loads 256 of the B columns (4 stages
-// of 48 KB).  A quarter fewer bytes cross from L2 per flop -- the measured limit of the 256 x
-// 256 tiles -- at the price of each tile's epilogue no longer overlapping the next tile's MMAs.
+// WIDE (pairs, problems of at least a full wave with beta = 0): 256 x 512 pair tiles, two
+// N = 256 MMAs per K step into one 512-column accumulator per CTA; each CTA loads 256 of the B
+// columns (4 stages of 48 KB).  A quarter fewer bytes cross from L2 per flop -- the measured
+// limit of the 256 x 256 tiles.  Each tile's epilogue no longer overlaps the next tile's
+// MMAs, so it only stages C and leaves the stores to the TMA unit (cp.async.bulk.tensor),
+// alternating two staging tiles per warp.
 //
 // The last, partial wave of tiles is split so that more SMs share it: into K halves whose
 // fp32 partial sums are exchanged (each half finishes half of the tile's columns), or into
@@ -90,8 +92,11 @@ struct Ring {
     static constexpr int kBStageBytes = kBRows * BK * 2;  // 16 KB or 32 KB
     static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
     static constexpr int kSideBytes = LDG ? (BM + kBRows) * 16 : 0;  // per stage
+    // TMA-read forms: two staging tiles per epilogue warp (TMA stores of C alternate between
+    // them); the loader form stores C with plain stores from one
+    static constexpr int kEpiBytes = LDG ? EPI_BYTES : 2 * EPI_BYTES;
     static constexpr int kSmemBytes =
-        kStages * (kStageBytes + kSideBytes) + EPI_BYTES + kBarBytes + 1024;  // + alignment slack
+        kStages * (kStageBytes + kSideBytes) + kEpiBytes + kBarBytes + 1024;  // + alignment slack
 };
 static_assert(Ring<true, false, true>::kSmemBytes <= 227 * 1024 &&
                   Ring<true>::kSmemBytes <= 227 * 1024 && Ring<false>::kSmemBytes <= 227 * 1024 &&
@@ -135,6 +140,7 @@ struct HgemmParams {
     uint32_t ab_format;        // instruction-descriptor input type: 0 = fp16, 1 = bf16
     int log_group;             // raster group of 2^log_group tile (pair) rows
     int tile_n;                // columns of a tile: 256, or 512 for the wide pair tiles
+    int c_tma;                 // beta == 0, TMA-read operands: C is written by TMA stores through map_c
     // Operands the tensor-memory-access unit cannot read (base not 16-byte aligned, leading
     // dimension or batch stride not a multiple of 8 elements) are read by the loader warps:
     // pointer, leading dimension and batch stride of the stored matrix, in elements.
@@ -275,6 +281,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Store of a box of shared memory at `src` to a 3-D tensor (C), tracked by this thread's bulk
+// async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 // The same copy issued by a CTA of a two-CTA pair whose completion is counted on an
@@ -671,7 +687,8 @@ template <int A_MN, int B_MN, bool PAIR, bool LDG, bool WIDE = false>
 __global__ void __launch_bounds__(threads_of<LDG>(), 1)
 hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_b_half,
-                     const __grid_constant__ CUtensorMap map_b_quarter, const HgemmParams p)
+                     const __grid_constant__ CUtensorMap map_b_quarter,
+                     const __grid_constant__ CUtensorMap map_c, const HgemmParams p)
 {
     static_assert(!WIDE || (PAIR && !LDG), "wide tiles: pairs of TMA-read operands");
     using R = Ring<PAIR, LDG, WIDE>;
@@ -689,7 +706,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
     const uint32_t sA = base;                                // STAGES x 16 KB
     const uint32_t sB = base + STAGES * A_STAGE_BYTES;       // STAGES x (16 or 32) KB
     float4 *epi_tiles = reinterpret_cast<float4 *>(smem + STAGES * R::kStageBytes);
-    uint8_t *bar_area = smem + STAGES * R::kStageBytes + EPI_BYTES;
+    uint8_t *bar_area = smem + STAGES * R::kStageBytes + R::kEpiBytes;
     const uint32_t bar0 = smem_u32(bar_area);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -1011,6 +1028,7 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
         const int quarter = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int cbuf = 0;  // with TMA stores: the staging tile of the next chunk
         const float alpha = p.alpha, beta = p.beta;
         for (int64_t u = unit0; u < p.num_units; u += ustride) {
             const Unit x = decode_unit(p, u);
@@ -1033,11 +1051,32 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             // this lane's row.  The rows go through the warp's staging tile (16-byte chunks
             // XOR-swizzled by row: conflict-free both ways), so that each store instruction
             // writes four 128-byte row segments instead of 32 scattered 16-byte pieces.
-            float4 *tile = epi_tiles + quarter * 256;
+            float4 *tile = epi_tiles + quarter * 256 * (LDG ? 1 : 2);
             const int64_t row0 = tm * BM + quarter * 32;  // first row of this warp
             auto store_chunk = [&](int c, const float *v) {
                 const int64_t gn0 = tn * p.tile_n + n_off + c * 32;
                 if (gn0 >= p.N) return;  // the same for the whole warp
+                if (!LDG && p.c_tma) {
+                    // beta == 0: alpha * acc into one of the warp's two staging tiles (laid out
+                    // as the tensor map's 128-byte swizzle), then one lane stores the 32 x 32
+                    // box by TMA (clipped at the edges of C) while the warp goes on
+                    float4 *tb = tile + 256 * cbuf;
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();  // the store that last read this tile has read it
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        tb[lane * 8 + (j ^ (lane & 7))] = make_float4(alpha * v[4 * j], alpha * v[4 * j + 1],
+                                                                      alpha * v[4 * j + 2], alpha * v[4 * j + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&map_c, smem_u32(tb), static_cast<int32_t>(gn0), static_cast<int32_t>(row0),
+                                     static_cast<int32_t>(bt));
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                    cbuf ^= 1;
+                    return;
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     tile[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -1184,6 +1223,8 @@ hgemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_con
             }
             if (++acc == kAccs) { acc = 0; acc_phase ^= 1u; }
         }
+        // every TMA store of C has completed (and read its staging tile) before the CTA ends
+        if (!LDG && p.c_tma && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
     __syncwarp();
@@ -1234,8 +1275,27 @@ bool make_map(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t cols,
 }
 
 struct Maps {
-    CUtensorMap a, b, b_half, b_quarter;
+    CUtensorMap a, b, b_half, b_quarter, c;
 };
+
+// 3-D tensor map over `batch` row-major fp32 matrices M x N (leading dimension ldc, `bstride`
+// elements apart) written in 32 x 32 boxes with the 128-byte swizzle (the layout of the
+// epilogue's staging tiles).
+bool make_map_c(CUtensorMap *map, float *ptr, int64_t M, int64_t N, int64_t ldc, int64_t batch, int64_t bstride)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const bool single = bstride == 0 || batch <= 1;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(single ? 1 : batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc) * 4,
+                                   static_cast<cuuint64_t>(single ? ldc * M : bstride) * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
 
 // Largest number of two-CTA clusters of the pair kernel that can be resident at once (0: none).
 template <int A_MN, int B_MN, bool LDG, bool WIDE = false>
@@ -1296,22 +1356,25 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         pair = max_clusters > 0;
     }
     // Wide pair tiles (256 x 512): a quarter less L2-to-SM traffic per flop, but the single
-    // 512-column accumulator leaves each tile's epilogue exposed.  Used when the problem has
-    // at least three full waves of them and beta == 0 (an epilogue that also reads C costs
-    // more than the saving: 16384 x 4096 x 4096 with beta = 1 ran 21% slower, 8192^3 with
-    // beta = 0 2-3.5% faster); GEMM_GB300_HGEMM_WIDE=0 never, =1 whenever pairs are used (for
-    // tests).
+    // 512-column accumulator leaves each tile's epilogue exposed.  Used when beta == 0 and C
+    // can be written by TMA stores (16-byte aligned, ldc and batch stride multiples of 4), so
+    // the epilogue hands its stores to the TMA unit and returns the accumulator quickly, and
+    // when there is at least one full wave of wide tiles (measured: 8192^3 +7%, 4096^3 +2%;
+    // with beta = 1 and plain stores 16384 x 4096 x 4096 ran 21% slower).
+    // GEMM_GB300_HGEMM_WIDE=0 never, =1 whenever pairs are used (for tests).
     if (!LDG && pair && p.tile_n == BN) {
         const char *wide_env = std::getenv("GEMM_GB300_HGEMM_WIDE");
         const char want = wide_env && wide_env[0] ? wide_env[0] : 'a';
         const int64_t per_batch_w = ((p.tiles_m + 1) / 2) * ((p.N + 2 * BN - 1) / (2 * BN));
         const int64_t work_w = per_batch_w * p.batch;
-        if (want != '0' && (want == '1' || (p.beta == 0.0f && work_w >= 3 * int64_t(max_clusters))) &&
+        const bool c_tma_ok = p.c_tma != 0;
+        if (want != '0' && (want == '1' || (c_tma_ok && work_w >= int64_t(max_clusters))) &&
             set_smem_attr<A_MN, B_MN, true, false, true>(dev.device) == cudaSuccess) {
             const int max_w = max_pair_clusters<A_MN, B_MN, false, true>(dev.device);
             if (max_w > 0) {
                 p.tile_n = 2 * BN;
                 p.tiles_n = (p.N + 2 * BN - 1) / (2 * BN);
+                const Maps &mw = m;
                 p.per_batch = per_batch_w;
                 p.full_tiles = work_w;
                 p.num_units = work_w;
@@ -1329,8 +1392,8 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
                 attr.val.clusterDim.z = 1;
                 cfg.attrs = &attr;
                 cfg.numAttrs = 1;
-                const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true, false, true>, m.a,
-                                                         m.b, m.b_half, m.b_quarter, p);
+                const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true, false, true>, mw.a,
+                                                         mw.b, mw.b_half, mw.b_quarter, mw.c, p);
                 if (e == cudaSuccess) count_launches();
                 return e;
             }
@@ -1370,7 +1433,7 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
         if (e != cudaSuccess) return e;
         hgemm_tcgen05_kernel<A_MN, B_MN, false, LDG>
             <<<static_cast<unsigned>(workers), threads_of<LDG>(), Ring<false, LDG>::kSmemBytes, stream>>>(
-                m.a, m.b, m.b_half, m.b_quarter, p);
+                m.a, m.b, m.b_half, m.b_quarter, m.c, p);
         const cudaError_t le = cudaGetLastError();
         if (le == cudaSuccess) count_launches();
         return le;
@@ -1388,7 +1451,7 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, hgemm_tcgen05_kernel<A_MN, B_MN, true, LDG>, m.a, m.b, m.b_half,
-                                             m.b_quarter, p);
+                                             m.b_quarter, m.c, p);
     if (e == cudaSuccess) count_launches();
     return e;
 }
@@ -1428,6 +1491,13 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
                make_map(&m.b_quarter, B, N, K, ldb, BK, BN / 4, batch, strideB, bf);
     }
     if (!ok_a || !ok_b) return GEMM_ERR_MISALIGNED;
+    const bool c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (batch <= 1 || strideC % 4 == 0);
+    // beta == 0 with operands read by TMA: the epilogue writes C by TMA stores.  Only when N is
+    // a multiple of 4 as well: a store box cut by the right edge of C is written in whole
+    // 16-byte pieces (measured: with N = 383 and ldc = 384 the padding column 383 was written),
+    // so every piece must lie inside or outside C.
+    const bool c_tma = !a_ldg && !b_ldg && beta == 0.0f && c_vec && N % 4 == 0 &&
+                       make_map_c(&m.c, C, M, N, ldc, batch, batch > 1 ? strideC : 0);
 
     HgemmParams p{};
     p.M = M; p.N = N; p.K = K;
@@ -1444,6 +1514,7 @@ gemm_status_t launch_hgemm(const DeviceInfo &dev, int dtype, int opA, int opB, i
     p.stride_c = batch > 1 ? strideC : 0;
     p.ab_format = bf ? 1u : 0u;
     p.tile_n = BN;
+    p.c_tma = c_tma;
     p.a_ldg = a_ldg;
     p.b_ldg = b_ldg;
     p.a_ptr = A;

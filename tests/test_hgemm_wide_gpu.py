@@ -33,21 +33,34 @@ def _pad8(cols):
     return (-cols) % 8
 
 
+@pytest.mark.parametrize("beta", [-0.5, 0.0])
 @pytest.mark.parametrize("opA,opB", list(itertools.product("NT", "NT")))
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_wide_tiles_full_oracle_and_same_bits(opA, opB, dtype, monkeypatch):
+def test_wide_tiles_full_oracle_and_same_bits(opA, opB, dtype, beta, monkeypatch):
     # 6 pair rows (the last one half outside M), N = 1240: 3 wide tiles, the last cut at 216
-    # columns; ragged K; padded C rows that must stay untouched
+    # columns; ragged K; padded C rows that must stay untouched.  beta = 0 with ldc a multiple
+    # of 4 writes C through TMA stores (clipped at the edges of C).
     M, N, K = 1408 + 77, 1240, 904
     w0 = workloads.Workload("probe", dtype, M, N, K, opA, opB)
-    w = workloads.Workload(f"wide_{dtype}_{opA}{opB}", dtype, M, N, K, opA, opB, alpha=1.25, beta=-0.5,
-                           seed=81, pad=(_pad8(w0.a_shape[1]), _pad8(w0.b_shape[1]), 3))
+    w = workloads.Workload(f"wide_{dtype}_{opA}{opB}", dtype, M, N, K, opA, opB, alpha=1.25, beta=beta,
+                           seed=81, pad=(_pad8(w0.a_shape[1]), _pad8(w0.b_shape[1]), 3 if beta else 4))
     inputs = workloads.make_inputs(w)
     wide = _run(w, inputs, monkeypatch, "1")
     narrow = _run(w, inputs, monkeypatch, "0")
     assert torch.equal(wide[:, : w.N].contiguous().view(torch.int32), narrow[:, : w.N].contiguous().view(torch.int32))
     assert torch.isnan(wide[:, w.N:]).all()  # row padding of C never written
     parity.check_full(w, inputs, wide[:, : w.N].contiguous())
+
+
+def test_edge_of_c_not_a_multiple_of_four_columns(monkeypatch):
+    # beta = 0, C aligned, ldc = 384 but N = 383: the last 16-byte piece of each row straddles
+    # the edge, so C is written without TMA stores; the padding column must stay untouched
+    w = workloads.Workload("c_edge_383", "f16", 65, 383, 8, alpha=-0.5, seed=84, pad=(0, 1, 1))
+    inputs = workloads.make_inputs(w)
+    for wide in ("0", "1"):
+        out = _run(w, inputs, monkeypatch, wide)
+        assert torch.isnan(out[:, w.N:]).all()
+        parity.check_full(w, inputs, out[:, : w.N].contiguous())
 
 
 def test_wide_tiles_integer_bit_exact_several_per_cluster(monkeypatch):
