@@ -1358,17 +1358,26 @@ cudaError_t launch_t(const DeviceInfo &dev, const Maps &m, HgemmParams p, cudaSt
     // Wide pair tiles (256 x 512): a quarter less L2-to-SM traffic per flop, but the single
     // 512-column accumulator leaves each tile's epilogue exposed.  Used when beta == 0 and C
     // can be written by TMA stores (16-byte aligned, ldc and batch stride multiples of 4), so
-    // the epilogue hands its stores to the TMA unit and returns the accumulator quickly, and
-    // when there is at least one full wave of wide tiles (measured: 8192^3 +7%, 4096^3 +2%;
-    // with beta = 1 and plain stores 16384 x 4096 x 4096 ran 21% slower).
+    // the epilogue hands its stores to the TMA unit and returns the accumulator quickly (with
+    // beta = 1 and plain stores 16384 x 4096 x 4096 ran 21% slower), when there is at least one
+    // full wave of wide tiles, and when their waves take no longer than the 256 x 256 tiles'.
+    // A wide tile costs 1.75 pair tiles (measured: 4096^3 1.75, 8192^3 1.79); the pair tiles'
+    // partial last wave costs half a tile in K halves (below), a whole one otherwise; the wide
+    // tiles' last wave is not split.  So 8192^3 takes wide tiles (7 waves, 12.25 pair-tile
+    // times against 13.5), 4096 x 2560 does not (2 waves, 3.5 against 2.5).
     // GEMM_GB300_HGEMM_WIDE=0 never, =1 whenever pairs are used (for tests).
     if (!LDG && pair && p.tile_n == BN) {
         const char *wide_env = std::getenv("GEMM_GB300_HGEMM_WIDE");
         const char want = wide_env && wide_env[0] ? wide_env[0] : 'a';
         const int64_t per_batch_w = ((p.tiles_m + 1) / 2) * ((p.N + 2 * BN - 1) / (2 * BN));
         const int64_t work_w = per_batch_w * p.batch;
+        const int64_t wc = max_clusters;
+        const int64_t work_n = ((p.tiles_m + 1) / 2) * p.tiles_n * p.batch;
+        const int64_t full_n = work_n / wc, tail_n = work_n % wc;
+        const double waves_n = double(full_n) + (tail_n == 0 ? 0.0 : (2 * tail_n <= wc && p.num_kb >= 8) ? 0.5 : 1.0);
+        const double waves_w = 1.75 * double((work_w + wc - 1) / wc);
         const bool c_tma_ok = p.c_tma != 0;
-        if (want != '0' && (want == '1' || (c_tma_ok && work_w >= int64_t(max_clusters))) &&
+        if (want != '0' && (want == '1' || (c_tma_ok && work_w >= wc && waves_w <= waves_n)) &&
             set_smem_attr<A_MN, B_MN, true, false, true>(dev.device) == cudaSuccess) {
             const int max_w = max_pair_clusters<A_MN, B_MN, false, true>(dev.device);
             if (max_w > 0) {
