@@ -99,9 +99,10 @@ GEMM_API gemm_status_t gemm_sgemm_f32(gemm_op_t opA, gemm_op_t opB, int64_t M, i
  * A, B: IEEE binary16 bit patterns (uint16_t), 2-byte aligned, any lda, ldb; an odd byte
  * address gives GEMM_ERR_MISALIGNED.  The tensor-memory-access unit reads rows only from a
  * 16-byte aligned base with a leading dimension that is a multiple of 8 elements; an operand
- * laid out otherwise is read by four loader warps of the same kernel instead (cp.async
- * copies where its rows are 4-byte aligned, loads through registers where they are only
- * 2-byte aligned), with no extra launch and no scratch memory.
+ * laid out otherwise is read by loader warps of the same kernel instead (each row copied as
+ * the aligned 16-byte blocks that cover it, then shifted into place in shared memory; rows
+ * at the ends of the operand's storage or cut by the matrix edge element by element), with
+ * no extra launch and no scratch memory, at a fraction of the TMA path's rate.
  * C: fp32, 4-byte aligned, any ldc.
  * Limits: M, N, K < 2^31; lda, ldb < 2^35 elements.
  */

@@ -2,9 +2,11 @@
 
 TMA copies rows only from a 16-byte aligned base with a leading dimension (and batch stride)
 that is a multiple of 8 elements.  Any other 2-byte aligned operand is read by the loader
-warps of the same kernel: cp.async copies of 16, 8 or 4 bytes where a row is that aligned,
-loads through registers where it is only 2-byte aligned, zero fill at the matrix edges.
-Each case is compared with the CPU oracle element by element.
+warps of the same kernel: each row is copied as the aligned 16-byte blocks that cover it
+(cp.async) and shifted into place in shared memory where it starts off a 16-byte boundary;
+rows at the ends of the operand's storage or cut by the matrix edge are read element by
+element, with zero fill outside the matrix.  Each case is compared with the CPU oracle
+element by element.
 """
 import itertools
 
@@ -48,8 +50,8 @@ def _run(w, inputs, off_a=0, off_b=0, calls=1):
 # alignment of the rows the loader warps see.
 LAYOUTS = {
     "odd_ld": ((1, 3), (0, 0)),          # rows alternate 2- and 4-byte alignment (and all classes mod 16)
-    "ld_4byte": ((2, 6), (0, 0)),        # rows 4-byte aligned: 4-byte cp.async
-    "ld_8byte": ((4, 4), (0, 0)),        # rows 8-byte aligned: 8-byte cp.async
+    "ld_4byte": ((2, 6), (0, 0)),        # rows 4-byte aligned (shifted by 4, 8 or 12 bytes)
+    "ld_8byte": ((4, 4), (0, 0)),        # rows 8-byte aligned (shifted by 8 bytes on odd rows)
     "base_2byte": ((0, 0), (1, 1)),      # aligned leading dimensions, every row 2-byte aligned
     "base_odd_ld": ((1, 1), (3, 1)),     # both
     "a_only": ((1, 0), (0, 0)),          # A through the loader, B by TMA
